@@ -1,0 +1,239 @@
+"""GB300 (sm_103a) attention hot path of a MiniMax-H3-style DiT block.
+
+Thin Python binding over ``libh3attn.so`` (C ABI in ``include/h3attn.h``).
+The functions here only check and marshal torch tensors into the C calls of
+the same names; every step of the path runs in the library's CUDA kernels.
+There is no fallback: if the library is missing or the device is not an
+sm_103 GPU, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "H3AttnError", "load_library", "library_path",
+    "h3attn_qk_norm_rope", "h3attn_forward", "h3attn_seq2head", "h3attn_head2seq",
+    "h3attn_get_device_status", "h3attn_strerror", "h3attn_version", "h3attn_selftest_wait_timeout",
+    "h3attn_last_device_error_info",
+    "ulysses_attention_step",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libh3attn.so")
+_lib = None
+
+H3ATTN_OK = 0
+H3ATTN_ERR_ARG = -1
+H3ATTN_ERR_SHAPE = -2
+H3ATTN_ERR_ALIAS = -3
+H3ATTN_ERR_CUDA = -4
+H3ATTN_ERR_DEVICE_TIMEOUT = -5
+H3ATTN_ERR_UNSUPPORTED_DEVICE = -6
+
+# exported symbol -> (restype, argtypes)
+_P, _I, _F, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
+SIGNATURES = {
+    "h3attn_qk_norm_rope": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P]),
+    "h3attn_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
+    "h3attn_seq2head": (_I, [_P, _P, _I, _I, _I, _I, _P]),
+    "h3attn_head2seq": (_I, [_P, _P, _I, _I, _I, _I, _P]),
+    "h3attn_get_device_status": (_I, [_P]),
+    "h3attn_last_device_error_info": (_U64, []),
+    "h3attn_last_cuda_error": (_I, []),
+    "h3attn_strerror": (ctypes.c_char_p, [_I]),
+    "h3attn_version": (_I, []),
+    "h3attn_selftest_wait_timeout": (_I, [_U64, _P]),
+}
+
+
+class H3AttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        msg = f"{fn} failed: {code} ({h3attn_strerror(code)})"
+        if code == H3ATTN_ERR_CUDA:
+            msg += f"; cudaError {load_library().h3attn_last_cuda_error()}"
+        super().__init__(msg)
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libh3attn.so (built in-tree by ``dit_sequence_attention_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is not built; run `python -m dit_sequence_attention_gb300.build` "
+                               "(or __graft_entry__.build()) first")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != H3ATTN_OK:
+        raise H3AttnError(fn, rc)
+
+
+def _bf16(t: torch.Tensor, name: str, device=None):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _bshd(t: torch.Tensor, name: str):
+    if t.dim() == 3:
+        return (1, *t.shape)
+    if t.dim() == 4:
+        return tuple(t.shape)
+    raise ValueError(f"{name} must be [S, H, D] or [B, S, H, D]")
+
+
+def h3attn_strerror(code: int) -> str:
+    return load_library().h3attn_strerror(int(code)).decode()
+
+
+def h3attn_version() -> int:
+    return int(load_library().h3attn_version())
+
+
+def h3attn_qk_norm_rope(q, k, q_out, k_out, w_q, w_k, pos, d_t, d_h, d_w, eps=1e-6, theta=10000.0,
+                        dbg_fp32=None, stream=None):
+    """QK-RMSNorm then 3-axis RoPE of q and k ([S,H,D] or [B,S,H,D] bf16); in place if q_out is q."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (q_out, "q_out"), (k_out, "k_out")):
+        _bf16(t, n, q.device)
+    B, S, H, D = _bshd(q, "q")
+    for t, n in ((k, "k"), (q_out, "q_out"), (k_out, "k_out")):
+        if _bshd(t, n) != (B, S, H, D):
+            raise ValueError(f"{n} shape {tuple(t.shape)} != q shape {tuple(q.shape)}")
+    for t, n in ((w_q, "w_q"), (w_k, "w_k")):
+        if t.dtype != torch.float32 or t.device != q.device or t.numel() != D or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous fp32 [D] tensor on {q.device}")
+    if pos.dtype != torch.int32 or pos.device != q.device or tuple(pos.shape) != (S, 3) or not pos.is_contiguous():
+        raise ValueError(f"pos must be a contiguous int32 [S, 3] tensor on {q.device}")
+    dbg = None
+    if dbg_fp32 is not None:
+        if dbg_fp32.dtype != torch.float32 or dbg_fp32.numel() != 2 * B * S * H * D or not dbg_fp32.is_contiguous():
+            raise ValueError("dbg_fp32 must be a contiguous fp32 tensor of 2*B*S*H*D elements")
+        dbg = dbg_fp32.data_ptr()
+    rc = lib.h3attn_qk_norm_rope(q.data_ptr(), k.data_ptr(), q_out.data_ptr(), k_out.data_ptr(), dbg,
+                                 w_q.data_ptr(), w_k.data_ptr(), pos.data_ptr(), B, S, H, D, d_t, d_h, d_w,
+                                 float(eps), float(theta), _stream_ptr(stream))
+    _check("h3attn_qk_norm_rope", rc)
+
+
+def h3attn_forward(q, k, v, o, head_begin=0, head_count=None, kv_len=None, scale=0.0, stream=None):
+    """Masked softmax attention for heads [head_begin, head_begin + head_count) of [B,]S,H_buf,D tensors.
+
+    kv_len: None (all S), an int (every batch item) or a sequence of B ints.
+    """
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _bf16(t, n, q.device)
+    B, S, H, D = _bshd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o")):
+        if _bshd(t, n) != (B, S, H, D):
+            raise ValueError(f"{n} shape {tuple(t.shape)} != q shape {tuple(q.shape)}")
+    if head_count is None:
+        head_count = H - head_begin
+    kv_arr = None
+    if kv_len is not None:
+        vals = [int(kv_len)] * B if isinstance(kv_len, int) else [int(x) for x in kv_len]
+        if len(vals) != B:
+            raise ValueError(f"kv_len has {len(vals)} entries, expected {B}")
+        kv_arr = (ctypes.c_int32 * B)(*vals)
+    rc = lib.h3attn_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, S, H, D,
+                            int(head_begin), int(head_count),
+                            ctypes.cast(kv_arr, ctypes.c_void_p) if kv_arr is not None else None,
+                            float(scale), _stream_ptr(stream))
+    _check("h3attn_forward", rc)
+
+
+def _layout(fn_name, src, dst, S, H, D, P, stream):
+    lib = load_library()
+    _bf16(src, "in")
+    _bf16(dst, "out", src.device)
+    if src.numel() != S * H * D or dst.numel() != S * H * D:
+        raise ValueError("in/out must hold S*H*D elements")
+    rc = getattr(lib, fn_name)(src.data_ptr(), dst.data_ptr(), S, H, D, int(P), _stream_ptr(stream))
+    _check(fn_name, rc)
+
+
+def h3attn_seq2head(x, out, P, stream=None):
+    """[S, H, D] (P sequence shards) -> out [P, S, H/P, D]."""
+    if x.dim() != 3:
+        raise ValueError("x must be [S, H, D]")
+    S, H, D = x.shape
+    _layout("h3attn_seq2head", x, out, S, H, D, P, stream)
+
+
+def h3attn_head2seq(x, out, P, stream=None):
+    """[P, S, H/P, D] -> out [S, H, D] (P sequence shards)."""
+    if x.dim() != 4 or x.shape[0] != P:
+        raise ValueError("x must be [P, S, H/P, D]")
+    _, S, Hp, D = x.shape
+    _layout("h3attn_head2seq", x, out, S, Hp * P, D, P, stream)
+
+
+def h3attn_get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code (0 = ok)."""
+    return int(load_library().h3attn_get_device_status(_stream_ptr(stream)))
+
+
+def h3attn_last_device_error_info() -> int:
+    return int(load_library().h3attn_last_device_error_info())
+
+
+def h3attn_selftest_wait_timeout(limit_ns: int, stream=None):
+    rc = load_library().h3attn_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream))
+    _check("h3attn_selftest_wait_timeout", rc)
+
+
+def ulysses_attention_step(q, k, v, w_q, w_k, pos, P, kv_len, d_t, d_h, d_w, eps=1e-6, theta=10000.0,
+                           work=None, stream=None):
+    """One pass of the whole hot path over [S, H, D] q, k, v with Ulysses degree P.
+
+    QK-norm + RoPE (in place into work buffers) -> seq2head of q', k', v ->
+    attention of each of the P head groups (one call per group, as each rank
+    of a P-way group would run it) -> head2seq of the output.  Returns o
+    [S, H, D].  `work` may pass preallocated buffers (dict with keys
+    'qr', 'kr', 'qh', 'kh', 'vh', 'oh', 'o') to keep allocation out of a timed loop.
+    """
+    S, H, D = q.shape
+    if work is None:
+        work = make_workspace(S, H, D, P, q.device)
+    qr, kr = work["qr"], work["kr"]
+    h3attn_qk_norm_rope(q, k, qr, kr, w_q, w_k, pos, d_t, d_h, d_w, eps, theta, stream=stream)
+    h3attn_seq2head(qr, work["qh"], P, stream)
+    h3attn_seq2head(kr, work["kh"], P, stream)
+    h3attn_seq2head(v, work["vh"], P, stream)
+    for g in range(P):
+        h3attn_forward(work["qh"][g], work["kh"][g], work["vh"][g], work["oh"][g],
+                       kv_len=kv_len, stream=stream)
+    h3attn_head2seq(work["oh"], work["o"], P, stream)
+    return work["o"]
+
+
+def make_workspace(S, H, D, P, device):
+    """Buffers for ulysses_attention_step (allocated once by the caller)."""
+    e = dict(dtype=torch.bfloat16, device=device)
+    return {"qr": torch.empty((S, H, D), **e), "kr": torch.empty((S, H, D), **e),
+            "qh": torch.empty((P, S, H // P, D), **e), "kh": torch.empty((P, S, H // P, D), **e),
+            "vh": torch.empty((P, S, H // P, D), **e), "oh": torch.empty((P, S, H // P, D), **e),
+            "o": torch.empty((S, H, D), **e)}

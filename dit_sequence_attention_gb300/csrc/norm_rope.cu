@@ -1,0 +1,158 @@
+// norm_rope.cu -- fused QK-RMSNorm + three-axis rotary embedding.
+//
+// "[feat] Tensor parallelism for MiniMax-H3" (diffusers PR #14609), PR
+// description: QK-norms are head_dim-shaped and applied after the head split;
+// the rotary embedding uses real sin/cos, broadcasts over heads, and its angle
+// is inv_freq times the position.  Per (token, head) row of q and of k:
+//     y = x / sqrt(mean(x^2) + eps) * w;   pair i of axis a rotated by pos_a * theta^(-2i/d_a).
+//
+// One block per token.  The token's D/2 rotation angles are shared by all
+// 2*H rows (q and k, every head), so the block computes cos/sin once: the
+// angle pos * inv_freq and its reduction to [-pi, pi] in fp64 (a handful of
+// fp64 ops per pair; the position is an exact integer, so the reduced angle
+// is accurate to ~1e-16 even for positions in the thousands), then sincosf on
+// the reduced fp32 angle.  Each thread owns 8 consecutive dims (one 16-byte
+// vector) of a row, i.e. 4 whole rotation pairs; the D/8 threads of a row
+// reduce the sum of squares with warp shuffles.  All loads of the token are
+// issued before any is used (up to 8 vectors per thread in flight).
+// HBM-bound: 4 * H * D * 2 bytes per token (read and write q and k).
+#include <cmath>
+#include <cstdint>
+
+#include "h3_device.cuh"
+#include "h3_internal.h"
+
+namespace h3 {
+
+constexpr int kNormThreads = 256;
+constexpr int kNormMaxVec = 8;  // vectors per thread held in registers per pass
+
+struct RopeTable {
+    double inv_freq[64];   // per rotation pair p = (global dim)/2
+    int axis[64];          // 0 = t, 1 = h, 2 = w
+};
+
+template <int D>
+__global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
+    const uint4* q, const uint4* k, uint4* qo, uint4* ko, float* __restrict__ dbg,
+    const float* __restrict__ wq, const float* __restrict__ wk, const int32_t* __restrict__ pos, int S, int H,
+    float eps, size_t dbg_k_offset, const RopeTable tab) {
+    constexpr int VPR = D / 8;  // vectors per row
+    constexpr double kTwoPi = 6.283185307179586476925286766559;
+    constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
+    __shared__ float2 cs[D / 2];
+
+    const int tok = blockIdx.x;  // b * S + s
+    const int s = tok % S;
+    if (threadIdx.x < D / 2) {
+        const int pr = threadIdx.x;
+        const double ang = static_cast<double>(__ldg(pos + 3 * s + tab.axis[pr])) * tab.inv_freq[pr];
+        const double turns = rint(ang * kInvTwoPi);
+        const float red = static_cast<float>(fma(-turns, kTwoPi, ang));
+        float sn, c;
+        sincosf(red, &sn, &c);
+        cs[pr] = make_float2(c, sn);
+    }
+    __syncthreads();
+
+    const int cpt = H * VPR;      // vectors per tensor for this token
+    const int total = 2 * cpt;
+    const int iters = (total + kNormThreads - 1) / kNormThreads;
+    const size_t tok_vec = static_cast<size_t>(tok) * cpt;
+    const float inv_d = 1.0f / static_cast<float>(D);
+
+    for (int it0 = 0; it0 < iters; it0 += kNormMaxVec) {
+        uint4 x[kNormMaxVec];
+#pragma unroll
+        for (int u = 0; u < kNormMaxVec; ++u) {
+            const int idx = (it0 + u) * kNormThreads + threadIdx.x;
+            if (it0 + u < iters && idx < total) {
+                const bool is_k = idx >= cpt;
+                const int c = is_k ? idx - cpt : idx;
+                x[u] = __ldcs((is_k ? k : q) + tok_vec + c);
+            } else {
+                x[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kNormMaxVec; ++u) {
+            if (it0 + u >= iters) break;  // uniform across the block
+            const int idx = (it0 + u) * kNormThreads + threadIdx.x;
+            const bool valid = idx < total;
+            const bool is_k = idx >= cpt;
+            const int c = is_k ? idx - cpt : idx;
+            const int part = c % VPR;
+            const uint32_t w4[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[2 * e] = bf16lo_to_f32(w4[e]);
+                f[2 * e + 1] = bf16hi_to_f32(w4[e]);
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+#pragma unroll
+            for (int off = VPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (!valid) continue;
+            const float inv = rsqrtf(ss * inv_d + eps);
+            const float4* wv = reinterpret_cast<const float4*>((is_k ? wk : wq) + part * 8);
+            const float4 wa = __ldg(wv), wb = __ldg(wv + 1);
+            const float wgt[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = f[e] * inv * wgt[e];
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const float2 r = cs[part * 4 + pp];
+                const float a = y[2 * pp], b = y[2 * pp + 1];
+                y[2 * pp] = a * r.x - b * r.y;
+                y[2 * pp + 1] = a * r.y + b * r.x;
+            }
+            uint4 out;
+            out.x = pack_bf16x2(y[0], y[1]);
+            out.y = pack_bf16x2(y[2], y[3]);
+            out.z = pack_bf16x2(y[4], y[5]);
+            out.w = pack_bf16x2(y[6], y[7]);
+            (is_k ? ko : qo)[tok_vec + c] = out;
+            if (dbg != nullptr) {
+                float4* d4 = reinterpret_cast<float4*>(dbg + (is_k ? dbg_k_offset : 0) + (tok_vec + c) * 8);
+                d4[0] = make_float4(y[0], y[1], y[2], y[3]);
+                d4[1] = make_float4(y[4], y[5], y[6], y[7]);
+            }
+        }
+    }
+}
+
+int launch_norm_rope(const void* q, const void* k, void* q_out, void* k_out, float* dbg, const float* w_q,
+                     const float* w_k, const int32_t* pos, int B, int S, int H, int D, int d_t, int d_h, int d_w,
+                     float eps, double theta, cudaStream_t stream) {
+    RopeTable tab;
+    const int width[3] = {d_t, d_h, d_w};
+    int pr = 0;
+    for (int a = 0; a < 3; ++a) {
+        for (int i = 0; i < width[a] / 2; ++i, ++pr) {
+            tab.inv_freq[pr] = std::pow(theta, -2.0 * static_cast<double>(i) / static_cast<double>(width[a]));
+            tab.axis[pr] = a;
+        }
+    }
+    for (; pr < 64; ++pr) {
+        tab.inv_freq[pr] = 0.0;
+        tab.axis[pr] = 0;
+    }
+    const size_t dbg_k = static_cast<size_t>(B) * S * H * D;
+    const unsigned blocks = static_cast<unsigned>(B) * static_cast<unsigned>(S);
+    if (blocks == 0) return H3ATTN_OK;
+    if (D == 128)
+        norm_rope_kernel<128><<<blocks, kNormThreads, 0, stream>>>(
+            static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<uint4*>(q_out),
+            static_cast<uint4*>(k_out), dbg, w_q, w_k, pos, S, H, eps, dbg_k, tab);
+    else
+        norm_rope_kernel<64><<<blocks, kNormThreads, 0, stream>>>(
+            static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<uint4*>(q_out),
+            static_cast<uint4*>(k_out), dbg, w_q, w_k, pos, S, H, eps, dbg_k, tab);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e);
+}
+
+}  // namespace h3

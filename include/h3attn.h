@@ -1,0 +1,162 @@
+/*
+ * h3attn.h -- C ABI of the GB300 (sm_103a) attention hot path of a
+ * MiniMax-H3-style video+audio DiT block:
+ *
+ *   QK-RMSNorm + 3-axis RoPE  ->  Ulysses seq->head layout  ->  exact masked
+ *   multi-head attention over the packed sequence  ->  head->seq layout.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors are row-major, token-major: [B][S][H][D] (batch, packed sequence,
+ *    head, head_dim), bf16 elements stored as raw 16-bit words.  head_dim D is
+ *    64 or 128; the head count is a runtime value, which is how a caller hands
+ *    the kernel a buffer that holds only 56/P heads (the diffusers TP PR
+ *    reshapes attention by the fixed head_dim and lets the head count follow).
+ *  - Every tensor pointer is a DEVICE pointer, 16-byte aligned.  The caller
+ *    owns all buffers; the library allocates no device memory per call.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls only enqueue work and return; nothing synchronises except
+ *    h3attn_get_device_status().
+ *  - Return value: H3ATTN_OK (0) or a negative H3ATTN_ERR_* code.  Arguments
+ *    are checked on the host before anything is launched; a rejected call
+ *    enqueues nothing.  No call traps or aborts the process.
+ *  - Device errors (a pipeline wait that ran out of time) are recorded in a
+ *    device status word and reported by h3attn_get_device_status().
+ */
+#ifndef H3ATTN_H
+#define H3ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define H3ATTN_VERSION 1
+
+#if defined(__GNUC__)
+#define H3ATTN_API __attribute__((visibility("default")))
+#else
+#define H3ATTN_API
+#endif
+
+enum h3attn_status {
+    H3ATTN_OK = 0,
+    H3ATTN_ERR_ARG = -1,            /* null/misaligned pointer, bad scalar (eps < 0, theta <= 0, ...) */
+    H3ATTN_ERR_SHAPE = -2,          /* unsupported or inconsistent sizes */
+    H3ATTN_ERR_ALIAS = -3,          /* output overlaps an input where that is not allowed */
+    H3ATTN_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed (see h3attn_last_cuda_error) */
+    H3ATTN_ERR_DEVICE_TIMEOUT = -5, /* a kernel gave up on a pipeline wait (device status word) */
+    H3ATTN_ERR_UNSUPPORTED_DEVICE = -6 /* current device is not an sm_103 (GB300-class) GPU */
+};
+
+/*
+ * h3attn_qk_norm_rope -- fused QK-RMSNorm and three-axis rotary embedding.
+ *
+ * Defined by "[feat] Tensor parallelism for MiniMax-H3" (diffusers PR #14609),
+ * PR description: the QK-norms are head_dim-shaped and applied after the head
+ * split; the rotary embedding uses real sin/cos, broadcasts over the head axis,
+ * and takes its angle as inv_freq times the position (loader-bug comment on
+ * the same page).  For every batch b, token s, head h and separately for q and k:
+ *     y[d]  = x[d] / sqrt(mean_e x[e]^2 + eps) * w[d]            (fp32)
+ *     axis a in (t, h, w) owns dims [off_a, off_a + d_a), off = (0, d_t, d_t + d_h);
+ *     pair i of axis a = dims (off_a + 2i, off_a + 2i + 1), angle = pos[s][a] * theta^(-2i/d_a);
+ *     (y0, y1) -> (y0 cos - y1 sin, y0 sin + y1 cos)
+ * then one round-to-nearest-even to bf16.  v is not touched.
+ *
+ *   q, k        [B][S][H][D] bf16 inputs.
+ *   q_out,k_out [B][S][H][D] bf16 outputs; may equal q / k (in place), must
+ *               not partially overlap them.
+ *   dbg_fp32    NULL, or [2][B][S][H][D] fp32 receiving the unrounded q then k
+ *               results (test aid).
+ *   w_q, w_k    [D] fp32 norm weights (shared by all heads).
+ *   pos         [S][3] int32 (t, h, w) positions, shared by all batch items.
+ *   d_t+d_h+d_w == D, each even.  eps >= 0, theta > 0.
+ */
+H3ATTN_API int h3attn_qk_norm_rope(const void* q, const void* k, void* q_out, void* k_out, float* dbg_fp32,
+                        const float* w_q, const float* w_k, const int32_t* pos, int B, int S, int H, int D,
+                        int d_t, int d_h, int d_w, float eps, float theta, void* stream);
+
+/*
+ * h3attn_forward -- exact softmax attention for a range of heads.
+ *
+ * Defined by "buqi-minimax-h3-multigpu" README, sections "On accuracy" and
+ * "How it works": every rank evaluates exact full attention over the whole
+ * packed sequence for its subset of the 56 heads.  Keys at positions >=
+ * kv_len[b] are padding (the sequence is padded to a multiple of 512; see the
+ * NKI note in the diffusers TP PR) and get weight exactly zero:
+ *     o[b][i][h] = sum_{j < kv_len[b]} softmax_j(scale * <q[b][i][h], k[b][j][h]>) v[b][j][h]
+ * for h in [head_begin, head_begin + head_count) and every query row i < S
+ * (padded query rows are computed like any other).  bf16 operands, fp32
+ * accumulation, the probabilities rounded to bf16 for the PV product, bf16
+ * output.  Heads outside the range are not written.
+ *
+ *   q, k, v, o  [B][S][H_buf][D] bf16; o must not overlap q, k or v.
+ *   kv_len      HOST array [B] with 1 <= kv_len[b] <= S, or NULL for all S.
+ *               Rows >= kv_len[b] of k and v are never read (NaN there is fine).
+ *   scale       softmax scale; <= 0 selects 1/sqrt(D).
+ * The per-head result does not depend on head_begin/head_count or on how many
+ * heads one call covers: splitting the heads over several calls gives
+ * bit-identical output.
+ */
+H3ATTN_API int h3attn_forward(const void* q, const void* k, const void* v, void* o, int B, int S, int H_buf, int D,
+                   int head_begin, int head_count, const int32_t* kv_len, float scale, void* stream);
+
+/*
+ * h3attn_seq2head -- Ulysses sequence->head exchange as a single-GPU layout
+ * transform ("buqi-minimax-h3-multigpu" README, "How it works": the sequence
+ * is row-sharded over P ranks for per-token work; attention needs every row
+ * for 56/P heads, so an all-to-all regroups q, k and v by head).
+ *     in  [P][S/P][H][D]  (the P sequence shards, i.e. one [S][H][D] tensor)
+ *     out [P][S][H/P][D]  out[g][s][j] = in[s / (S/P)][s % (S/P)][g*(H/P) + j]
+ * Pure 16-bit word movement (bit-exact).  S % P == 0, H % P == 0, P >= 1.
+ * in and out must not overlap.
+ */
+H3ATTN_API int h3attn_seq2head(const void* in, void* out, int S, int H, int D, int P, void* stream);
+
+/*
+ * h3attn_head2seq -- the inverse exchange (the attention output all-to-all,
+ * "How it works" of the same README):
+ *     in  [P][S][H/P][D]  ->  out [P][S/P][H][D],
+ *     out[r][i][g*(H/P) + j] = in[g][r*(S/P) + i][j].
+ * head2seq(seq2head(x)) == x bit for bit.  in and out must not overlap.
+ */
+H3ATTN_API int h3attn_head2seq(const void* in, void* out, int S, int H, int D, int P, void* stream);
+
+/*
+ * h3attn_get_device_status -- synchronise `stream`, then read and clear the
+ * device status word of the current device.  Returns H3ATTN_OK,
+ * H3ATTN_ERR_DEVICE_TIMEOUT (a kernel gave up on a wait, wrote nothing
+ * trustworthy and returned), or H3ATTN_ERR_CUDA if the synchronisation itself
+ * failed.
+ */
+H3ATTN_API int h3attn_get_device_status(void* stream);
+
+/* Diagnostic word recorded with the last device error (kernel tag << 32 |
+ * wait site << 16 | block index), 0 if none.  Read after h3attn_get_device_status. */
+H3ATTN_API unsigned long long h3attn_last_device_error_info(void);
+
+/* cudaError_t value behind the most recent H3ATTN_ERR_CUDA on this thread. */
+H3ATTN_API int h3attn_last_cuda_error(void);
+
+/* Static description of a status code. */
+H3ATTN_API const char* h3attn_strerror(int code);
+
+/* H3ATTN_VERSION of the built library. */
+H3ATTN_API int h3attn_version(void);
+
+/*
+ * h3attn_selftest_wait_timeout -- failure-detection self-test.  Launches one
+ * block whose wait on an mbarrier that nothing ever arrives on uses the same
+ * bounded wait as the attention pipeline, with a limit of `limit_ns`
+ * nanoseconds (1 <= limit_ns <= 10^10).  The wait runs out, the kernel records
+ * H3ATTN_ERR_DEVICE_TIMEOUT and returns; the next h3attn_get_device_status()
+ * reports it and the context stays usable.
+ */
+H3ATTN_API int h3attn_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3ATTN_H */

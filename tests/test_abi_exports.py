@@ -1,0 +1,92 @@
+"""The C-ABI library builds, loads without a GPU and exports every symbol that
+include/h3attn.h declares; host-side argument checks run before any CUDA call.
+No GPU needed (no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dit_sequence_attention_gb300 import build
+    build.build()
+    import dit_sequence_attention_gb300 as h3
+    return h3.load_library()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "h3attn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(h3attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("h3attn_qk_norm_rope", "h3attn_forward", "h3attn_seq2head", "h3attn_head2seq",
+                     "h3attn_get_device_status", "h3attn_strerror"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import dit_sequence_attention_gb300 as h3
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared but not exported"
+        assert name in h3.SIGNATURES, f"{name} has no Python binding"
+
+
+def test_no_undeclared_exports():
+    # every exported h3attn_* symbol must be declared in the header
+    import subprocess
+    import dit_sequence_attention_gb300 as h3
+    out = subprocess.run(["nm", "-D", "--defined-only", h3.library_path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\b(h3attn_\w+)$", out, flags=re.M))
+    assert exported == set(declared_functions())
+
+
+def test_version_and_strerror_need_no_gpu(lib):
+    assert lib.h3attn_version() == 1
+    assert lib.h3attn_strerror(0) == b"ok"
+    assert b"timeout" in lib.h3attn_strerror(-5)
+    assert lib.h3attn_strerror(12345) == b"unknown status"
+
+
+def test_argument_checks_run_before_any_cuda_call(lib):
+    import dit_sequence_attention_gb300 as h3
+    null = None
+    fake = 0x10000  # aligned, never dereferenced: the checks reject the call first
+    assert lib.h3attn_forward(null, fake, fake, fake, 1, 256, 4, 64, 0, 4, null, 0.0, null) == h3.H3ATTN_ERR_ARG
+    assert lib.h3attn_forward(fake, fake + 0x100000, fake + 0x200000, fake + 0x300000, 1, 256, 4, 96, 0, 4,
+                              null, 0.0, null) == h3.H3ATTN_ERR_SHAPE
+    assert lib.h3attn_forward(fake, fake + 0x100000, fake + 0x200000, fake + 0x300000, 1, 256, 4, 64, 2, 3,
+                              null, 0.0, null) == h3.H3ATTN_ERR_SHAPE
+    kv = (ctypes.c_int32 * 1)(0)
+    assert lib.h3attn_forward(fake, fake + 0x100000, fake + 0x200000, fake + 0x300000, 1, 256, 4, 64, 0, 4,
+                              ctypes.cast(kv, ctypes.c_void_p), 0.0, null) == h3.H3ATTN_ERR_SHAPE
+    assert lib.h3attn_forward(fake, fake, fake, fake, 1, 256, 4, 64, 0, 4, null, 0.0, null) == h3.H3ATTN_ERR_ALIAS
+    assert lib.h3attn_forward(fake + 8, fake + 0x100000, fake + 0x200000, fake + 0x300000, 1, 256, 4, 64, 0, 4,
+                              null, 0.0, null) == h3.H3ATTN_ERR_ARG
+    assert lib.h3attn_seq2head(fake, fake + 0x100000, 64, 56, 128, 3, null) == h3.H3ATTN_ERR_SHAPE
+    assert lib.h3attn_seq2head(fake, fake + 0x100, 64, 56, 128, 2, null) == h3.H3ATTN_ERR_ALIAS
+    assert lib.h3attn_head2seq(fake, fake + 0x100000, 63, 56, 128, 2, null) == h3.H3ATTN_ERR_SHAPE
+    # norm/rope: split must sum to D, even widths, eps >= 0, theta > 0
+    args = [fake, fake + 0x100000, fake + 0x200000, fake + 0x300000, null, fake + 0x400000, fake + 0x500000,
+            fake + 0x600000, 1, 16, 4, 64]
+    f = lib.h3attn_qk_norm_rope
+    assert f(*args, 16, 24, 22, 1e-6, 1e4, null) == h3.H3ATTN_ERR_SHAPE
+    assert f(*args, 15, 25, 24, 1e-6, 1e4, null) == h3.H3ATTN_ERR_SHAPE
+    assert f(*args, 16, 24, 24, -1.0, 1e4, null) == h3.H3ATTN_ERR_ARG
+    assert f(*args, 16, 24, 24, 1e-6, 0.0, null) == h3.H3ATTN_ERR_ARG
+    assert lib.h3attn_selftest_wait_timeout(0, null) == h3.H3ATTN_ERR_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import dit_sequence_attention_gb300 as h3
+    monkeypatch.setattr(h3, "_lib", None)
+    monkeypatch.setattr(h3, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        h3.load_library()

@@ -1,0 +1,231 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Bars (written in each test): layout permutations bit-exact; attention output
+within max-relative error 2e-2 per head (max |gpu - ref| / max |ref| over that
+head's rows and dims); fp32 norm/RoPE output within 1e-5 of the same ratio per
+tensor; bf16 norm/RoPE output within one bf16 ulp of the oracle value rounded
+to bf16.  All inputs are seeded draws from dit_sequence_attention_gb300.synth;
+no oracle input comes from the CUDA path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dit_sequence_attention_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+ATTN_TOL = 2e-2
+NORM_TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def h3(cuda_device):
+    from dit_sequence_attention_gb300 import build
+    build.build()
+    import dit_sequence_attention_gb300 as m
+    m.load_library()
+    return m
+
+
+def per_head_rel_err(got, ref):
+    """[rows, H, D] -> per-head max|got-ref| / max|ref|."""
+    return np.abs(got - ref).max(axis=(0, 2)) / np.abs(ref).max(axis=(0, 2))
+
+
+def bits(t):
+    return oracle.bf16_bits(t)
+
+
+# ------------------------------------------------------------------ layout
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("P", [1, 2, 4, 7, 8])
+def test_layout_bit_exact_vs_oracle(h3, cuda_device, P, D):
+    S, H = 56 * 9, 56
+    x = synth.randn_bf16((S, H, D), 11)
+    xd = x.to(cuda_device)
+    out = torch.empty((P, S, H // P, D), dtype=torch.bfloat16, device=cuda_device)
+    h3.h3attn_seq2head(xd, out, P)
+    back = torch.empty_like(xd)
+    h3.h3attn_head2seq(out, back, P)
+    assert h3.h3attn_get_device_status() == 0
+    np.testing.assert_array_equal(bits(out), oracle.seq2head(bits(x), P))
+    np.testing.assert_array_equal(bits(back), bits(x))
+
+
+def test_layout_rejects_bad_shapes_and_aliasing(h3, cuda_device):
+    x = torch.zeros((64, 56, 128), dtype=torch.bfloat16, device=cuda_device)
+    out = torch.empty((3, 64, 56 // 3, 128), dtype=torch.bfloat16, device=cuda_device)
+    lib = h3.load_library()
+    s = torch.cuda.current_stream().cuda_stream
+    assert lib.h3attn_seq2head(x.data_ptr(), out.data_ptr(), 64, 56, 128, 3, s) == h3.H3ATTN_ERR_SHAPE
+    assert lib.h3attn_seq2head(x.data_ptr(), x.data_ptr(), 64, 56, 128, 2, s) == h3.H3ATTN_ERR_ALIAS
+    assert lib.h3attn_seq2head(x.data_ptr() + 2, out.data_ptr(), 64, 56, 128, 2, s) == h3.H3ATTN_ERR_ARG
+    assert lib.h3attn_seq2head(x.data_ptr(), out.data_ptr(), 64, 56, 96, 2, s) == h3.H3ATTN_ERR_SHAPE
+
+
+# -------------------------------------------------------------- norm + rope
+def _norm_rope_case(h3, dev, w, S=None):
+    S = S or w.S
+    shape = (S, w.H, w.D)
+    q, k = synth.randn_bf16(shape, synth.SEED_Q), synth.randn_bf16(shape, synth.SEED_K)
+    wq, wk = synth.norm_weights(w.D)
+    pos = synth.packed_positions(w)[:S]
+    qo = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    ko = torch.empty_like(qo)
+    dbg = torch.empty((2,) + shape, dtype=torch.float32, device=dev)
+    h3.h3attn_qk_norm_rope(q.to(dev), k.to(dev), qo, ko, wq.to(dev), wk.to(dev), torch.from_numpy(pos).to(dev),
+                           *w.rope_split, w.eps, w.theta, dbg_fp32=dbg)
+    assert h3.h3attn_get_device_status() == 0
+    refs = [oracle.norm_rope(oracle.bf16_to_f64(t), wt.double().numpy(), pos, w.eps, *w.rope_split, w.theta)
+            for t, wt in ((q, wq), (k, wk))]
+    return (qo, ko), dbg.cpu().numpy(), refs
+
+
+@pytest.mark.parametrize("name", ["tiny", "c2"])
+def test_norm_rope_matches_oracle(h3, cuda_device, name):
+    w = synth.WORKLOADS[name]
+    outs, dbg, refs = _norm_rope_case(h3, cuda_device, w)
+    for i in range(2):
+        ref = refs[i]
+        err = np.abs(dbg[i] - ref).max() / np.abs(ref).max()
+        assert err <= NORM_TOL, f"fp32 norm/rope rel err {err:.3e} > {NORM_TOL}"
+        # bf16 output: within one bf16 ulp of the oracle rounded to bf16
+        got = outs[i].float().cpu().numpy().astype(np.float64)
+        ref_b = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref_b), 2.0 ** -126))) - 7)
+        assert np.all(np.abs(got - ref_b) <= ulp), "bf16 norm/rope output off by more than one ulp"
+
+
+def test_norm_rope_in_place_equals_out_of_place(h3, cuda_device):
+    w = synth.WORKLOADS["c2"]
+    S = 512
+    shape = (S, w.H, w.D)
+    q, k = synth.randn_bf16(shape, 5, cuda_device), synth.randn_bf16(shape, 6, cuda_device)
+    wq, wk = (t.to(cuda_device) for t in synth.norm_weights(w.D))
+    pos = torch.from_numpy(synth.packed_positions(w)[:S]).to(cuda_device)
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    h3.h3attn_qk_norm_rope(q, k, qo, ko, wq, wk, pos, *w.rope_split)
+    q2, k2 = q.clone(), k.clone()
+    h3.h3attn_qk_norm_rope(q2, k2, q2, k2, wq, wk, pos, *w.rope_split)
+    assert torch.equal(q2, qo) and torch.equal(k2, ko)
+
+
+# ---------------------------------------------------------------- attention
+def _attn(h3, dev, S, H, D, kv, seed=21, rows=None, heads=None):
+    q, k, v = (synth.randn_bf16((S, H, D), seed + i) for i in range(3))
+    o = torch.empty((S, H, D), dtype=torch.bfloat16, device=dev)
+    h3.h3attn_forward(q.to(dev), k.to(dev), v.to(dev), o, kv_len=kv)
+    assert h3.h3attn_get_device_status() == 0
+    rows = np.arange(S) if rows is None else np.asarray(rows)
+    heads = np.arange(H) if heads is None else np.asarray(heads)
+    qf = oracle.bf16_to_f64(q)[rows][:, heads]
+    kf, vf = oracle.bf16_to_f64(k)[:, heads], oracle.bf16_to_f64(v)[:, heads]
+    ref = oracle.attention(qf, kf, vf, kv_len=kv)
+    got = o.float().cpu().numpy()[rows][:, heads]
+    return got, ref
+
+
+@pytest.mark.parametrize("S,H,D,kv", [
+    (256, 4, 64, 256),      # tiny workload shape, one query block, two key tiles
+    (256, 4, 64, 200),      # ragged key tail inside the second tile
+    (700, 3, 128, 333),     # ragged query tail (700 = 2*256 + 188) and key tail
+    (300, 2, 64, 1),        # a single valid key
+    (128, 2, 128, 128),     # second query tile entirely out of range
+    (1000, 2, 128, 1000),   # eight key tiles, last partial
+])
+def test_attention_matches_oracle(h3, cuda_device, S, H, D, kv):
+    got, ref = _attn(h3, cuda_device, S, H, D, kv)
+    err = per_head_rel_err(got, ref)
+    assert np.all(err <= ATTN_TOL), f"per-head rel err {err}"
+
+
+def test_attention_c2_workload_sampled_rows(h3, cuda_device):
+    w = synth.WORKLOADS["c2"]
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([rng.choice(w.S, 192, replace=False), [0, 127, 128, 255, 4039, 4040, 4095]]))
+    got, ref = _attn(h3, cuda_device, w.S, w.H, w.D, w.S_v, rows=rows)
+    err = per_head_rel_err(got, ref)
+    assert np.all(err <= ATTN_TOL), f"per-head rel err max {err.max():.3e}"
+
+
+def test_attention_head_groups_bit_identical_to_all_heads(h3, cuda_device):
+    S, H, D, kv = 1024, 56, 128, 1000
+    q, k, v = (synth.randn_bf16((S, H, D), 40 + i, cuda_device) for i in range(3))
+    full = torch.empty_like(q)
+    h3.h3attn_forward(q, k, v, full, kv_len=kv)
+    for P in (2, 4, 7, 8):
+        part = torch.full_like(q, float("nan"))
+        for g in range(P):
+            h3.h3attn_forward(q, k, v, part, head_begin=g * H // P, head_count=H // P, kv_len=kv)
+        assert torch.equal(part.view(torch.int16), full.view(torch.int16)), f"P={P} differs"
+
+
+def test_attention_masked_keys_never_read(h3, cuda_device):
+    S, H, D, kv = 512, 2, 128, 377
+    q, k, v = (synth.randn_bf16((S, H, D), 60 + i, cuda_device) for i in range(3))
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    h3.h3attn_forward(q, k, v, o1, kv_len=kv)
+    k2, v2 = k.clone(), v.clone()
+    k2[kv:] = float("nan")
+    v2[kv:] = float("nan")
+    h3.h3attn_forward(q, k2, v2, o2, kv_len=kv)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert not torch.isnan(o2).any()
+
+
+def test_attention_uniform_values(h3, cuda_device):
+    S, H, D = 512, 2, 128
+    q, k = synth.randn_bf16((S, H, D), 70, cuda_device), synth.randn_bf16((S, H, D), 71, cuda_device)
+    row = synth.randn_bf16((1, H, D), 72, cuda_device)
+    v = row.expand(S, H, D).contiguous()
+    o = torch.empty_like(q)
+    h3.h3attn_forward(q, k, v, o, kv_len=450)
+    err = (o.float() - v.float()).abs().max() / v.float().abs().max()
+    assert err <= 2 ** -8, f"uniform V rel err {err}"
+
+
+def test_attention_argument_errors(h3, cuda_device):
+    x = torch.zeros((256, 4, 64), dtype=torch.bfloat16, device=cuda_device)
+    o = torch.empty_like(x)
+    with pytest.raises(h3.H3AttnError) as e:
+        h3.h3attn_forward(x, x, x, o, head_begin=3, head_count=2)
+    assert e.value.code == h3.H3ATTN_ERR_SHAPE
+    with pytest.raises(h3.H3AttnError) as e:
+        h3.h3attn_forward(x, x, x, o, kv_len=257)
+    assert e.value.code == h3.H3ATTN_ERR_SHAPE
+    with pytest.raises(h3.H3AttnError) as e:
+        h3.h3attn_forward(x, x, x, x)
+    assert e.value.code == h3.H3ATTN_ERR_ALIAS
+
+
+# ------------------------------------------------------------- whole path
+@pytest.mark.parametrize("P", [1, 2, 4])
+def test_pipeline_c2_matches_oracle(h3, cuda_device, P):
+    w = synth.WORKLOADS["c2"]
+    q, k, v = synth.qkv(w)
+    wq, wk = synth.norm_weights(w.D)
+    pos = synth.packed_positions(w)
+    dev = cuda_device
+    o = h3.ulysses_attention_step(q.to(dev), k.to(dev), v.to(dev), wq.to(dev), wk.to(dev),
+                                  torch.from_numpy(pos).to(dev), P, w.S_v, *w.rope_split, w.eps, w.theta)
+    assert h3.h3attn_get_device_status() == 0
+    heads = np.array([0, 13, 27, 28, 41, 55])
+    rows = np.unique(np.concatenate([np.arange(0, w.S, 37), [w.S_v - 1, w.S_v, w.S - 1]]))
+    qf = oracle.norm_rope(oracle.bf16_to_f64(q)[:, heads], wq.double().numpy(), pos, w.eps, *w.rope_split, w.theta)
+    kf = oracle.norm_rope(oracle.bf16_to_f64(k)[:, heads], wk.double().numpy(), pos, w.eps, *w.rope_split, w.theta)
+    ref = oracle.attention(qf[rows], kf, oracle.bf16_to_f64(v)[:, heads], kv_len=w.S_v)
+    got = o.float().cpu().numpy()[rows][:, heads]
+    err = per_head_rel_err(got, ref)
+    assert np.all(err <= ATTN_TOL), f"P={P}: per-head rel err {err}"
+
+
+def test_device_timeout_is_reported_and_context_survives(h3, cuda_device):
+    assert h3.h3attn_get_device_status() == 0
+    h3.h3attn_selftest_wait_timeout(2_000_000)  # 2 ms wait on a barrier nothing arrives on
+    assert h3.h3attn_get_device_status() == h3.H3ATTN_ERR_DEVICE_TIMEOUT
+    assert (h3.h3attn_last_device_error_info() >> 32) == 2
+    assert h3.h3attn_get_device_status() == 0  # cleared
+    x = torch.ones(1024, device=cuda_device)
+    assert float(x.sum()) == 1024.0
