@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Benchmark of the H3 attention hot path on GB300.
+
+One step = one pass of the whole path over one packed sequence (batch 1):
+QK-RMSNorm + 3-axis RoPE of q and k, Ulysses seq->head of q', k', v with
+degree P, attention of each of the P head groups (one h3attn_forward call per
+group, as each rank of a P-way group would issue it), head->seq of the output.
+
+The default workload is the 480p-like packed sequence: 56 heads x 128,
+49,920 video tokens (32 x 30 x 52) + 992 audio tokens padded to 51,200 keys
+with a key-padding mask.  Inputs are seeded synthetic N(0,1) bf16 (no dataset,
+no trained weights); each tensor is 734 MB, larger than L2, so no L2 flush is
+needed between steps.
+
+Output: ONE JSON line on rank 0.  `value` is attention TFLOP/s over the whole
+job: 4 * S_v^2 * D * H per sequence (valid tokens only), summed over ranks,
+divided by the max-over-ranks wall time of the timed steps.
+
+--impl reference times the fp64 CPU oracle (the plain definition of the same
+computation) on the host cores, on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs its own independent sequence (weak
+scaling, no data-path collective); torch.distributed is used only for the
+barrier and the max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("attention TFLOPS & tokens/s at 56 heads×128, 50k-262k tokens; % of bf16 peak")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_dram_traffic.txt")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["h3attn", "reference"], default="h3attn")
+    ap.add_argument("--workload", default="480p", choices=["c2", "16k", "480p", "1080p"])
+    ap.add_argument("--P", type=int, default=2, help="Ulysses degree emulated inside one step")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            flat = {}
+
+            def walk(x, prefix=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, f"{prefix}{k}.")
+                elif isinstance(x, (int, float)):
+                    flat[prefix[:-1]] = float(x)
+            walk(d)
+
+            def pick(*names):
+                for n in names:
+                    for k, v in flat.items():
+                        if k.split(".")[-1] == n:
+                            return v
+                return None
+            hbm = pick("hbm_gbs", "hbm_GBps", "copy_gbs")
+            b = pick("bf16_tflops", "bf16_tflops_burst")
+            bs = pick("bf16_tflops_sustained")
+            if hbm and b:
+                return {"hbm_gbs": hbm, "bf16_tflops": b, "bf16_tflops_sustained": bs or b}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def read_traffic():
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu summary, if any."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if line.startswith("traffic_bytes_per_launch_480p_group28:"):
+                try:
+                    return float(line.split(":", 1)[1].split()[0])
+                except ValueError:
+                    return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv", "-lms", "200"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        with open(self.path) as f:
+            text = f.read()
+        os.unlink(self.path)
+        rows = list(csv.reader(io.StringIO(text)))
+        if len(rows) < 2:
+            return None
+        hdr = [h.strip() for h in rows[0]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows[1:]:
+            if len(r) != len(hdr):
+                continue
+            rec = dict(zip(hdr, [x.strip() for x in r]))
+            try:
+                sm.append(float(rec[[h for h in hdr if h.startswith("clocks.current.sm") or h.startswith("clocks.sm")][0]].split()[0]))
+                smax.append(float(rec[[h for h in hdr if h.startswith("clocks.max.sm")][0]].split()[0]))
+            except Exception:
+                continue
+            for n in names:
+                key = [h for h in hdr if h.startswith(f"clocks_event_reasons.{n}")]
+                if key and rec[key[0]].lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if args.impl == "h3attn" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def cpu_oracle_sample(w, target_s, seed_offset=0):
+    """Time the fp64 oracle on a bounded sample of workload `w`: QK-norm + RoPE of
+    the sampled heads' keys and query rows, then attention of the sampled rows
+    against every valid key.  Returns (flops_attention, seconds, description, threads)."""
+    import numpy as np
+    import oracle
+    from dit_sequence_attention_gb300 import synth
+    oracle.build()
+    rng = np.random.default_rng(7 + seed_offset)
+    pos = synth.packed_positions(w)
+    wq, wk = synth.norm_weights(w.D)
+    wq64, wk64 = wq.double().numpy(), wk.double().numpy()
+    # one head's q/k/v (per-head draws keep host memory small; the oracle sees bf16-exact values)
+    gen = lambda seed: synth.randn_bf16((w.S, 1, w.D), 1000 + seed + seed_offset, zero_rows_from=w.S_v)
+    qh, kh, vh = (oracle.bf16_to_f64(gen(s)) for s in (1, 2, 3))
+
+    def run(rows):
+        t0 = time.perf_counter()
+        kr = oracle.norm_rope(kh, wk64, pos, w.eps, *w.rope_split, w.theta)
+        qr = oracle.norm_rope(qh[rows], wq64, pos[rows], w.eps, *w.rope_split, w.theta)
+        oracle.attention(qr, kr, vh, kv_len=w.S_v)
+        return time.perf_counter() - t0
+
+    rows = np.sort(rng.choice(w.S, 16, replace=False))
+    t_small = run(rows)
+    n = int(min(w.S, max(16, 16 * target_s / max(t_small, 1e-3))))
+    rows = np.sort(rng.choice(w.S, n, replace=False))
+    dt = run(rows)
+    flops = 4.0 * n * w.S_v * w.D
+    desc = (f"1 head x {n} sampled query rows (QK-norm+RoPE of those rows and all {w.S} keys, "
+            f"then attention over {w.S_v} valid keys) of the {w.name} workload")
+    return flops, dt, desc, oracle.num_threads()
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the fp64 CPU oracle on the host cores, rank 0 only."""
+    from dit_sequence_attention_gb300 import synth
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    per_step = max(2.0, min(20.0, 100.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        cpu_oracle_sample(w, per_step / 4, seed_offset=i)
+    flops, secs = 0.0, 0.0
+    desc, threads = "", 0
+    for i in range(args.steps):
+        f, dt, desc, threads = cpu_oracle_sample(w, per_step, seed_offset=100 + i)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, args.P),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {desc}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, P):
+    return {"workload": f"{w.name}-like packed sequence: {w.n_video} video tokens "
+                        f"({w.frames}x{w.grid_h}x{w.grid_w}) + {w.n_audio} audio tokens, padded to {w.S} "
+                        f"with masked keys; 56 heads x 128; QK-norm+RoPE -> Ulysses seq2head (P={P}) -> "
+                        f"attention per head group -> head2seq",
+            "S": w.S, "S_valid": w.S_v, "heads": w.H, "head_dim": w.D, "batch_per_gpu": 1,
+            "ulysses_P": P, "l2": f"inputs larger than L2 ({w.S * w.H * w.D * 2 / 1e6:.0f} MB per tensor); no flush"}
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import numpy as np
+    import torch
+    import dit_sequence_attention_gb300 as h3
+    from dit_sequence_attention_gb300 import synth
+
+    h3.load_library()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    P = args.P
+    S, H, D = w.S, w.H, w.D
+    # each rank draws its own sequence (independent problems, weak scaling)
+    q, k, v = (synth.randn_bf16((S, H, D), seed + 1000 * rank, dev, zero_rows_from=w.S_v)
+               for seed in (synth.SEED_Q, synth.SEED_K, synth.SEED_V))
+    wq, wk = (t.to(dev) for t in synth.norm_weights(D))
+    pos = torch.from_numpy(synth.packed_positions(w)).to(dev)
+    work = h3.make_workspace(S, H, D, P, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = {"norm": [], "s2h": [], "attn": [], "h2s": []}
+
+    def step(record=False):
+        def mark():
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            return e
+        e0 = mark() if record else None
+        h3.h3attn_qk_norm_rope(q, k, work["qr"], work["kr"], wq, wk, pos, *w.rope_split, w.eps, w.theta)
+        e1 = mark() if record else None
+        h3.h3attn_seq2head(work["qr"], work["qh"], P)
+        h3.h3attn_seq2head(work["kr"], work["kh"], P)
+        h3.h3attn_seq2head(v, work["vh"], P)
+        e2 = mark() if record else None
+        marks = []
+        for g in range(P):
+            h3.h3attn_forward(work["qh"][g], work["kh"][g], work["vh"][g], work["oh"][g], kv_len=w.S_v)
+            if record:
+                marks.append(mark())
+        h3.h3attn_head2seq(work["oh"], work["o"], P)
+        e4 = mark() if record else None
+        if record:
+            ev["norm"].append((e0, e1))
+            ev["s2h"].append((e1, e2))
+            prev = e2
+            for m in marks:
+                ev["attn"].append((prev, m))
+                prev = m
+            ev["h2s"].append((marks[-1], e4))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if h3.h3attn_get_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    clocks = ClockSampler(local) if rank == 0 or True else None
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    status = h3.h3attn_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    def avg(name):
+        xs = [a.elapsed_time(b) for a, b in ev[name]]
+        return sum(xs) / len(xs)
+
+    flops_seq = w.attention_flops()
+    total_flops = flops_seq * args.steps * world
+    value = total_flops / (elapsed_ms * 1e-3) / 1e12
+    ms_step = elapsed_ms / args.steps
+    attn_ms = avg("attn")                                   # per launch (one head group)
+    flops_launch = w.attention_flops(heads=H // P)
+    achieved = flops_launch / (attn_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops_sustained"]
+    traffic = read_traffic() if (P == 2 and w.name == "480p") else None
+    tensor_bytes = S * H * D * 2
+    kernels = {
+        "qk_norm_rope": {"ms": avg("norm"), "GB_per_s": 4 * tensor_bytes / (avg("norm") * 1e-3) / 1e9},
+        "seq2head_x3": {"ms": avg("s2h"), "GB_per_s": 6 * tensor_bytes / (avg("s2h") * 1e-3) / 1e9},
+        "attention_per_group": {"ms": attn_ms, "TFLOP_per_s": achieved},
+        "head2seq": {"ms": avg("h2s"), "GB_per_s": 2 * tensor_bytes / (avg("h2s") * 1e-3) / 1e9},
+    }
+    hbm_peak = peaks["hbm_gbs"]
+    for kname in ("qk_norm_rope", "seq2head_x3", "head2seq"):
+        kernels[kname]["frac_of_hbm_peak"] = kernels[kname]["GB_per_s"] / hbm_peak
+
+    # ---------------------------------------------------------------- e2e
+    e2e_steps = args.e2e_steps or max(2, min(args.steps, 5))
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    hpos = pos.cpu().pin_memory()
+    ho = torch.empty((S, H, D), dtype=torch.bfloat16).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dpos = torch.empty_like(pos)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dpos.copy_(hpos, non_blocking=True)
+        o = h3.ulysses_attention_step(dq, dk, dv, wq, wk, dpos, P, w.S_v, *w.rope_split, w.eps, w.theta,
+                                      work=work)
+        ho.copy_(o, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = a.elapsed_time(b)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = flops_seq * e2e_steps * world / (e2e_ms * 1e-3) / 1e12
+    h2d = 3 * tensor_bytes + hpos.numel() * 4
+    d2h = tensor_bytes
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        f, dt, desc, threads = cpu_oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v, random-init norm weights)",
+        "config": workload_config(w, P),
+        "tokens_per_s": w.S_v * args.steps * world / (elapsed_ms * 1e-3),
+        "frac_of_bf16_peak": value / peak,
+        "roofline": {"kernel": "attn_fwd_kernel<128> (one 28-head group launch)" if D == 128 else "attn_fwd_kernel",
+                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 dense, sustained",
+                     "burst_peak": peaks["bf16_tflops"], "frac_of_burst": achieved / peaks["bf16_tflops"],
+                     "algorithmic_flops_per_launch": flops_launch},
+        "kernels": kernels,
+        "hbm_peak_GB_per_s": hbm_peak,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps},
+        "gpu_launches": args.steps * (1 + 3 + P + 1),
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -61,6 +61,10 @@ WORKLOADS = {
     # 8x16x30 video + 200 audio = 4040 valid, padded to 4096.
     "c2": Workload("c2", H=56, D=128, frames=8, grid_h=16, grid_w=30,
                    n_audio=200, S=4096),
+    # 16x30x32 video + 992 audio = 16,352 valid, padded to 16,384: a profiling-size
+    # case whose tensors (235 MB each) still exceed L2.
+    "16k": Workload("16k", H=56, D=128, frames=16, grid_h=30, grid_w=32,
+                    n_audio=992, S=16384),
     # 32x30x52 video + 992 audio = 50,912 valid, padded to 51,200.
     "480p": Workload("480p", H=56, D=128, frames=32, grid_h=30, grid_w=52,
                      n_audio=992, S=51200),
