@@ -11,6 +11,8 @@
 //   warp 9      allocates 512 TMEM columns, one lane issues every tcgen05.mma:
 //               S_i = Q_i K^T (both operands in shared memory) and
 //               O_i += P_i V   (P from TMEM, V from shared memory, MN-major).
+//               Shared-memory descriptors are built once; each K=16 step adds a
+//               compile-time offset, so issue keeps pace with the 64-cycle MMA.
 //   warps 0-3   softmax for query tile 0 (rows 0..127), warps 4-7 for tile 1.
 //               Thread = one query row = one TMEM lane: row max, exp2, row sum
 //               with no shuffles; P is written back over S as bf16 pairs; O is
@@ -33,35 +35,46 @@ namespace h3 {
 constexpr int kAttnThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
+#ifndef H3_ATTN_KSTAGES
+#define H3_ATTN_KSTAGES 3
+#endif
+#ifndef H3_ATTN_VSTAGES
+#define H3_ATTN_VSTAGES 2
+#endif
+
 template <int D>
 struct AttnTraits {
     static constexpr int BM = 128;                       // query rows per tile (TMEM lanes)
     static constexpr int BN = 128;                       // keys per tile
+    static constexpr int KST = H3_ATTN_KSTAGES;          // key ring depth
+    static constexpr int VST = H3_ATTN_VSTAGES;          // value ring depth
     static constexpr int NCHUNK = D / 64;                // 128-byte swizzle boxes along head_dim
     static constexpr int CHUNK_BYTES = 128 * 128;        // 128 rows x 64 bf16
     static constexpr int TILE_BYTES = NCHUNK * CHUNK_BYTES;
     static constexpr int OFF_Q = 0;                      // 2 query tiles
-    static constexpr int OFF_K = 2 * TILE_BYTES;         // 2 key stages
-    static constexpr int OFF_V = 4 * TILE_BYTES;         // 2 value stages
-    static constexpr int OFF_BAR = 6 * TILE_BYTES;
+    static constexpr int OFF_K = 2 * TILE_BYTES;         // KST key stages
+    static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;  // VST value stages
+    static constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
     static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // barriers + 1 KB alignment slack
+    static_assert(KST >= 2 && KST <= 4 && VST >= 2 && VST <= 4, "ring depth");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per block");
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);
 };
 
-// Barrier slots (8 bytes each) in the barrier area.
+// Barrier slots (8 bytes each) in the barrier area (room for up to 4 stages per ring).
 enum : int {
     B_QFULL = 0,
-    B_KFULL = 1,   // +stage
-    B_VFULL = 3,   // +stage
-    B_KEMPTY = 5,  // +stage
-    B_VEMPTY = 7,  // +stage
-    B_SFULL = 9,   // +query tile
-    B_PFULL = 11,  // +query tile
-    B_OFINAL = 13, // +query tile
-    B_DRAIN = 15,
-    B_COUNT = 16
+    B_KFULL = 1,    // +stage
+    B_VFULL = 5,    // +stage
+    B_KEMPTY = 9,   // +stage
+    B_VEMPTY = 13,  // +stage
+    B_SFULL = 17,   // +query tile
+    B_PFULL = 19,   // +query tile
+    B_OFINAL = 21,  // +query tile
+    B_DRAIN = 23,
+    B_COUNT = 24
 };
 
 struct AttnParams {
@@ -85,24 +98,28 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     }
 }
 
+// Issue S = Q K^T: eight K=16 steps.  The descriptors are built once per CTA;
+// each step only adds a compile-time offset to the start-address field, so
+// the single issuing thread keeps up with the tensor core (rebuilding a
+// descriptor per instruction costs more than the 64-cycle MMA itself).
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sQ, uint32_t sK) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
     using T = AttnTraits<D>;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * T::CHUNK_BYTES + (kk % 4) * 32;
-        mma_ss(d_tmem, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024), T::IDESC_QK,
-               kk > 0 ? 1u : 0u);
+        const uint64_t off = static_cast<uint64_t>(((kk / 4) * T::CHUNK_BYTES + (kk % 4) * 32) >> 4);
+        mma_ss(d_tmem, dq + off, dk + off, T::IDESC_QK, kk > 0 ? 1u : 0u);
     }
 }
 
+// Issue O (+)= P V: eight K=16 steps over the tile's 128 keys.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t sV, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t dv, bool accumulate) {
     using T = AttnTraits<D>;
 #pragma unroll
     for (int kk = 0; kk < T::BN / 16; ++kk) {
         // 16 keys per instruction: P columns (bf16 pairs) [8kk, 8kk+8), V rows [16kk, 16kk+16).
-        mma_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(sV + kk * 2048, T::CHUNK_BYTES, 1024), T::IDESC_PV,
+        mma_ts(d_tmem, p_tmem + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), T::IDESC_PV,
                (accumulate || kk > 0) ? 1u : 0u);
     }
 }
@@ -129,14 +146,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_QFULL), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < T::KST; ++s) {
             mbar_init(bar(B_KFULL + s), 1);
-            mbar_init(bar(B_VFULL + s), 1);
             mbar_init(bar(B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < T::VST; ++s) {
+            mbar_init(bar(B_VFULL + s), 1);
             mbar_init(bar(B_VEMPTY + s), 1);
-            mbar_init(bar(B_SFULL + s), 1);
-            mbar_init(bar(B_PFULL + s), 128);
-            mbar_init(bar(B_OFINAL + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(B_SFULL + t), 1);
+            mbar_init(bar(B_PFULL + t), 128);
+            mbar_init(bar(B_OFINAL + t), 1);
         }
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
@@ -164,74 +185,79 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (lane == 0) {
             const uint64_t keep = l2_policy_evict_last();   // K/V: reused by every query block of the head
             const uint64_t once = l2_policy_evict_first();  // Q: read once
-            int last_use[2][2] = {{-1, -1}, {-1, -1}};      // [K/V][stage] -> last issued use
+            int last_k = -1, last_v = -1;                   // last tile index issued per ring
             mbar_arrive_expect_tx(bar(B_QFULL), 2 * T::TILE_BYTES);
             for (int t = 0; t < 2; ++t)
                 for (int c = 0; c < T::NCHUNK; ++c)
                     tma_load_3d_hint(sQ + t * T::TILE_BYTES + c * T::CHUNK_BYTES, &tmQ, bar(B_QFULL), c * 64,
                                      head, q0 + t * T::BM, once);
-            bool ok = true;
-            for (int j = 0; j < n && ok; ++j) {
-                const int s = j & 1, u = j >> 1;
-                if (u > 0 && !mbar_wait(bar(B_KEMPTY + s), (u - 1) & 1, ctl, 1)) { ok = false; break; }
-                mbar_arrive_expect_tx(bar(B_KFULL + s), T::TILE_BYTES);
+            for (int j = 0; j < n; ++j) {
+                const int ks = j % T::KST, ku = j / T::KST;
+                if (ku > 0 && !mbar_wait(bar(B_KEMPTY + ks), (ku - 1) & 1, ctl, 1)) break;
+                mbar_arrive_expect_tx(bar(B_KFULL + ks), T::TILE_BYTES);
                 for (int c = 0; c < T::NCHUNK; ++c)
-                    tma_load_3d_hint(sK + s * T::TILE_BYTES + c * T::CHUNK_BYTES, &tmK, bar(B_KFULL + s), c * 64,
+                    tma_load_3d_hint(sK + ks * T::TILE_BYTES + c * T::CHUNK_BYTES, &tmK, bar(B_KFULL + ks), c * 64,
                                      head, j * T::BN, keep);
-                last_use[0][s] = u;
-                if (u > 0 && !mbar_wait(bar(B_VEMPTY + s), (u - 1) & 1, ctl, 2)) { ok = false; break; }
-                mbar_arrive_expect_tx(bar(B_VFULL + s), T::TILE_BYTES);
+                last_k = j;
+                const int vs = j % T::VST, vu = j / T::VST;
+                if (vu > 0 && !mbar_wait(bar(B_VEMPTY + vs), (vu - 1) & 1, ctl, 2)) break;
+                mbar_arrive_expect_tx(bar(B_VFULL + vs), T::TILE_BYTES);
                 for (int c = 0; c < T::NCHUNK; ++c)
-                    tma_load_3d_hint(sV + s * T::TILE_BYTES + c * T::CHUNK_BYTES, &tmV, bar(B_VFULL + s), c * 64,
+                    tma_load_3d_hint(sV + vs * T::TILE_BYTES + c * T::CHUNK_BYTES, &tmV, bar(B_VFULL + vs), c * 64,
                                      head, j * T::BN, keep);
-                last_use[1][s] = u;
+                last_v = j;
             }
             if (*abort_flag) {  // let every copy already issued land before the CTA exits
                 const uint64_t lim = p.wait_limit_ns;
                 drain_wait(bar(B_QFULL), 0, lim);
-                for (int s = 0; s < 2; ++s) {
-                    if (last_use[0][s] >= 0) drain_wait(bar(B_KFULL + s), last_use[0][s] & 1, lim);
-                    if (last_use[1][s] >= 0) drain_wait(bar(B_VFULL + s), last_use[1][s] & 1, lim);
-                }
+                for (int j = last_k; j >= 0 && j > last_k - T::KST; --j)
+                    drain_wait(bar(B_KFULL + j % T::KST), (j / T::KST) & 1, lim);
+                for (int j = last_v; j >= 0 && j > last_v - T::VST; --j)
+                    drain_wait(bar(B_VFULL + j % T::VST), (j / T::VST) & 1, lim);
             }
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
+            const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t dQ1 = smem_desc_sw128(sQ + T::TILE_BYTES, 16, 1024);
+            const uint64_t dK = smem_desc_sw128(sK, 16, 1024);               // + stage * TILE_BYTES / 16
+            const uint64_t dV = smem_desc_sw128(sV, T::CHUNK_BYTES, 1024);   // + stage * TILE_BYTES / 16
+            constexpr uint64_t kStage = T::TILE_BYTES >> 4;
             bool ok = mbar_wait(bar(B_QFULL), 0, ctl, 10) && mbar_wait(bar(B_KFULL + 0), 0, ctl, 11);
             if (ok) {
                 tc_fence_after_sync();
-                issue_qk<D>(tmem + T::COL_S0, sQ, sK);
+                issue_qk<D>(tmem + T::COL_S0, dQ0, dK);
                 mma_commit(bar(B_SFULL + 0));
-                issue_qk<D>(tmem + T::COL_S1, sQ + T::TILE_BYTES, sK);
+                issue_qk<D>(tmem + T::COL_S1, dQ1, dK);
                 mma_commit(bar(B_SFULL + 1));
                 mma_commit(bar(B_KEMPTY + 0));
             }
             for (int j = 0; j < n && ok; ++j) {
-                const int vs = j & 1, vu = j >> 1;
+                const int vs = j % T::VST, vu = j / T::VST;
                 const bool more = (j + 1) < n;
-                const int ks = (j + 1) & 1, ku = (j + 1) >> 1;
-                const uint32_t sVj = sV + vs * T::TILE_BYTES;
+                const int ks = (j + 1) % T::KST, ku = (j + 1) / T::KST;
+                const uint64_t dVj = dV + vs * kStage;
                 if (!mbar_wait(bar(B_VFULL + vs), vu & 1, ctl, 12) || !mbar_wait(bar(B_PFULL + 0), j & 1, ctl, 13)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                issue_pv<D>(tmem + T::COL_O0, tmem + T::COL_S0, sVj, j > 0);
+                issue_pv<D>(tmem + T::COL_O0, tmem + T::COL_S0, dVj, j > 0);
                 if (more) {
                     if (!mbar_wait(bar(B_KFULL + ks), ku & 1, ctl, 14)) { ok = false; break; }
                     tc_fence_after_sync();
-                    issue_qk<D>(tmem + T::COL_S0, sQ, sK + ks * T::TILE_BYTES);
+                    issue_qk<D>(tmem + T::COL_S0, dQ0, dK + ks * kStage);
                     mma_commit(bar(B_SFULL + 0));
                 } else {
                     mma_commit(bar(B_OFINAL + 0));
                 }
                 if (!mbar_wait(bar(B_PFULL + 1), j & 1, ctl, 15)) { ok = false; break; }
                 tc_fence_after_sync();
-                issue_pv<D>(tmem + T::COL_O1, tmem + T::COL_S1, sVj, j > 0);
+                issue_pv<D>(tmem + T::COL_O1, tmem + T::COL_S1, dVj, j > 0);
                 mma_commit(bar(B_VEMPTY + vs));
                 if (more) {
-                    issue_qk<D>(tmem + T::COL_S1, sQ + T::TILE_BYTES, sK + ks * T::TILE_BYTES);
+                    issue_qk<D>(tmem + T::COL_S1, dQ1, dK + ks * kStage);
                     mma_commit(bar(B_SFULL + 1));
                     mma_commit(bar(B_KEMPTY + ks));
                 } else {
@@ -260,60 +286,69 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SFULL + wg), j & 1, ctl, 20 + wg))) { ok = false; break; }
             tc_fence_after_sync();
             float s[T::BN];
-#pragma unroll
-            for (int c = 0; c < T::BN / 32; ++c) {
-                float t32[32];
-                tmem_ld32(lane_addr + colS + 32 * c, t32);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[32 * c + i] = t32[i];
-            }
+            tmem_ld128(lane_addr + colS, s);
             if (j == n - 1 && tail < T::BN) {
 #pragma unroll
                 for (int c = 0; c < T::BN; ++c)
                     if (c >= tail) s[c] = -INFINITY;
             }
-            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+            // row max: eight independent chains of three-input max, then a tree
+            float mx[8];
 #pragma unroll
-            for (int c = 4; c < T::BN; c += 4) {
-                mx0 = fmaxf(mx0, s[c]);
-                mx1 = fmaxf(mx1, s[c + 1]);
-                mx2 = fmaxf(mx2, s[c + 2]);
-                mx3 = fmaxf(mx3, s[c + 3]);
+            for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+            for (int c = 16; c < T::BN; c += 16) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
             }
-            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
             const bool need = (j > 0) && (mt > m + kRescaleThreshold);
             if (__any_sync(0xffffffffu, need)) {
                 const float alpha = need ? ex2_approx(m - mt) : 1.0f;
+                const uint64_t alpha2 = f2_pack(alpha, alpha);
 #pragma unroll
                 for (int c = 0; c < D / 16; ++c) {
                     float o16[16];
                     uint32_t w16[16];
                     tmem_ld16(lane_addr + colO + 16 * c, o16);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w16[i] = __float_as_uint(o16[i] * alpha);
+                    for (int i = 0; i < 8; ++i) {
+                        float a, b;
+                        f2_unpack(f2_mul(f2_pack(o16[2 * i], o16[2 * i + 1]), alpha2), a, b);
+                        w16[2 * i] = __float_as_uint(a);
+                        w16[2 * i + 1] = __float_as_uint(b);
+                    }
                     tmem_st16(lane_addr + colO + 16 * c, w16);
                 }
                 tmem_wait_st();
                 l *= alpha;
             }
             if (j == 0 || need) m = mt;
-            const float neg_m = -m;
-            float l0 = 0.f, l1 = 0.f;
-            // P (bf16 pairs) overwrites the first BN/2 columns of S, 32 keys at a time.
+            // p = exp2(s * scale*log2e - m): the argument as packed fp32 pairs, the
+            // sums in four packed accumulators; P (bf16 pairs) overwrites the first
+            // BN/2 columns of S, 32 keys at a time (stores complete at the wait below).
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t negm2 = f2_pack(-m, -m);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int c = 0; c < T::BN / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2_approx(fmaf(s[32 * c + 2 * i], sl2, neg_m));
-                    const float p1 = ex2_approx(fmaf(s[32 * c + 2 * i + 1], sl2, neg_m));
-                    l0 += p0;
-                    l1 += p1;
+                    float a0, a1;
+                    f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, negm2), a0, a1);
+                    const float p0 = ex2_approx(a0);
+                    const float p1 = ex2_approx(a1);
+                    acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(lane_addr + colS + 16 * c, pk);
             }
-            l += l0 + l1;
+            {
+                float a0, a1;
+                f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+                l += a0 + a1;
+            }
             tmem_wait_st();
             tc_fence_before_sync();
             mbar_arrive(bar(B_PFULL + wg));
