@@ -11,11 +11,13 @@
 //   warp 9      allocates 512 TMEM columns, one lane issues every tcgen05.mma:
 //               S_i = Q_i K^T (both operands in shared memory) and
 //               O_i += P_i V   (P from TMEM, V from shared memory, MN-major).
-//               Shared-memory descriptors are built once; each K=16 step adds a
-//               compile-time offset, so issue keeps pace with the 64-cycle MMA.
 //   warps 0-3   softmax for query tile 0 (rows 0..127), warps 4-7 for tile 1.
-//               Thread = one query row = one TMEM lane: row max, exp2, row sum
-//               with no shuffles; P is written back over S as bf16 pairs; O is
+//               Thread = one query row = one TMEM lane: the 128 scores arrive in
+//               one 128-column TMEM load; row max with three-input max; then the
+//               exp2 arguments for the whole row (packed f32x2 FMA), all 128
+//               exponentials, and the packed sums and bf16 pairs -- phase-ordered
+//               so the exponentials run back to back on the MUFU pipe while the
+//               other pipes work; P is written back over S as bf16 pairs; O is
 //               rescaled in TMEM only when the running max grows by more than
 //               2^8 (otherwise the stale max is kept, which is exact after the
 //               final division).
@@ -329,24 +331,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // BN/2 columns of S, 32 keys at a time (stores complete at the wait below).
             const uint64_t sl2x2 = f2_pack(sl2, sl2);
             const uint64_t negm2 = f2_pack(-m, -m);
-            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+            // arguments for all 128 keys, then all exponentials, then sums and packs
+#pragma unroll
+            for (int i = 0; i < T::BN / 2; ++i) {
+                float a0, a1;
+                f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negm2), a0, a1);
+                s[2 * i] = a0;
+                s[2 * i + 1] = a1;
+            }
+#pragma unroll
+            for (int i = 0; i < T::BN; ++i) s[i] = ex2_approx(s[i]);
+            uint64_t acc[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int c = 0; c < T::BN / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    float a0, a1;
-                    f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, negm2), a0, a1);
-                    const float p0 = ex2_approx(a0);
-                    const float p1 = ex2_approx(a1);
-                    acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+                    const float p0 = s[32 * c + 2 * i], p1 = s[32 * c + 2 * i + 1];
+                    acc[i & 7] = f2_add(acc[i & 7], f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(lane_addr + colS + 16 * c, pk);
             }
             {
                 float a0, a1;
-                f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+                f2_unpack(f2_add(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])),
+                                 f2_add(f2_add(acc[4], acc[5]), f2_add(acc[6], acc[7]))), a0, a1);
                 l += a0 + a1;
             }
             tmem_wait_st();
