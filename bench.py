@@ -362,7 +362,7 @@ def main():
     achieved = flops_launch / (attn_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops_sustained"]
-    traffic = read_traffic() if (P == 2 and w.name == "480p") else None
+    traffic = read_traffic() if (P == 2 and w.name == "480p" and D == 128) else None
     tensor_bytes = S * H * D * 2
     kernels = {
         "qk_norm_rope": {"ms": avg("norm"), "GB_per_s": 4 * tensor_bytes / (avg("norm") * 1e-3) / 1e9},
