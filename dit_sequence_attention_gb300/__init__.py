@@ -15,7 +15,8 @@ import torch
 
 __all__ = [
     "H3AttnError", "load_library", "library_path",
-    "h3attn_qk_norm_rope", "h3attn_forward", "h3attn_seq2head", "h3attn_head2seq",
+    "h3attn_qk_norm_rope", "h3attn_qk_norm_rope_seq2head", "h3attn_forward", "h3attn_seq2head",
+    "h3attn_head2seq", "h3attn_head2seq_heads",
     "h3attn_get_device_status", "h3attn_strerror", "h3attn_version", "h3attn_selftest_wait_timeout",
     "h3attn_last_device_error_info",
     "ulysses_attention_step",
@@ -38,6 +39,8 @@ _P, _I, _F, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulong
 SIGNATURES = {
     "h3attn_qk_norm_rope": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P]),
     "h3attn_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
+    "h3attn_qk_norm_rope_seq2head": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P]),
+    "h3attn_head2seq_heads": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "h3attn_seq2head": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "h3attn_head2seq": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "h3attn_get_device_status": (_I, [_P]),
@@ -138,6 +141,36 @@ def h3attn_qk_norm_rope(q, k, q_out, k_out, w_q, w_k, pos, d_t, d_h, d_w, eps=1e
     _check("h3attn_qk_norm_rope", rc)
 
 
+def h3attn_qk_norm_rope_seq2head(q, k, qh_out, kh_out, w_q, w_k, pos, P, d_t, d_h, d_w, eps=1e-6,
+                                 theta=10000.0, dbg_fp32=None, stream=None):
+    """QK-norm + RoPE of [S,H,D] q and k written straight into the head-sharded [P,S,H/P,D] layout."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (qh_out, "qh_out"), (kh_out, "kh_out")):
+        _bf16(t, n, q.device)
+    if q.dim() != 3 or k.shape != q.shape:
+        raise ValueError("q and k must be [S, H, D] of the same shape")
+    S, H, D = q.shape
+    if H % P or S % P:
+        raise ValueError(f"P={P} must divide S={S} and H={H}")
+    for t, n in ((qh_out, "qh_out"), (kh_out, "kh_out")):
+        if tuple(t.shape) != (P, S, H // P, D):
+            raise ValueError(f"{n} must be [P, S, H/P, D] = {(P, S, H // P, D)}")
+    for t, n in ((w_q, "w_q"), (w_k, "w_k")):
+        if t.dtype != torch.float32 or t.device != q.device or t.numel() != D or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous fp32 [D] tensor on {q.device}")
+    if pos.dtype != torch.int32 or pos.device != q.device or tuple(pos.shape) != (S, 3) or not pos.is_contiguous():
+        raise ValueError(f"pos must be a contiguous int32 [S, 3] tensor on {q.device}")
+    dbg = None
+    if dbg_fp32 is not None:
+        if dbg_fp32.dtype != torch.float32 or dbg_fp32.numel() != 2 * S * H * D or not dbg_fp32.is_contiguous():
+            raise ValueError("dbg_fp32 must be a contiguous fp32 tensor of 2*S*H*D elements")
+        dbg = dbg_fp32.data_ptr()
+    rc = lib.h3attn_qk_norm_rope_seq2head(q.data_ptr(), k.data_ptr(), qh_out.data_ptr(), kh_out.data_ptr(), dbg,
+                                          w_q.data_ptr(), w_k.data_ptr(), pos.data_ptr(), S, H, D, int(P), d_t, d_h,
+                                          d_w, float(eps), float(theta), _stream_ptr(stream))
+    _check("h3attn_qk_norm_rope_seq2head", rc)
+
+
 def h3attn_forward(q, k, v, o, head_begin=0, head_count=None, kv_len=None, scale=0.0, stream=None):
     """Masked softmax attention for heads [head_begin, head_begin + head_count) of [B,]S,H_buf,D tensors.
 
@@ -191,6 +224,21 @@ def h3attn_head2seq(x, out, P, stream=None):
     _layout("h3attn_head2seq", x, out, S, Hp * P, D, P, stream)
 
 
+def h3attn_head2seq_heads(x_group, out, P, group, head_begin, head_count, stream=None):
+    """Heads [head_begin, head_begin+head_count) of group `group` ([S, H/P, D]) -> out [S, H, D]."""
+    lib = load_library()
+    _bf16(x_group, "in_group")
+    _bf16(out, "out", x_group.device)
+    if x_group.dim() != 3 or out.dim() != 3:
+        raise ValueError("in_group must be [S, H/P, D] and out [S, H, D]")
+    S, Hp, D = x_group.shape
+    if tuple(out.shape) != (S, Hp * P, D):
+        raise ValueError("out must be [S, H, D] with H = P * (H/P)")
+    rc = lib.h3attn_head2seq_heads(x_group.data_ptr(), out.data_ptr(), S, Hp * P, D, int(P), int(group),
+                                   int(head_begin), int(head_count), _stream_ptr(stream))
+    _check("h3attn_head2seq_heads", rc)
+
+
 def h3attn_get_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code (0 = ok)."""
     return int(load_library().h3attn_get_device_status(_stream_ptr(stream)))
@@ -206,34 +254,67 @@ def h3attn_selftest_wait_timeout(limit_ns: int, stream=None):
 
 
 def ulysses_attention_step(q, k, v, w_q, w_k, pos, P, kv_len, d_t, d_h, d_w, eps=1e-6, theta=10000.0,
-                           work=None, stream=None):
+                           work=None, stream=None, fused=True, attn_chunks=1, exchange_stream=None):
     """One pass of the whole hot path over [S, H, D] q, k, v with Ulysses degree P.
 
-    QK-norm + RoPE (in place into work buffers) -> seq2head of q', k', v ->
-    attention of each of the P head groups (one call per group, as each rank
-    of a P-way group would run it) -> head2seq of the output.  Returns o
-    [S, H, D].  `work` may pass preallocated buffers (dict with keys
-    'qr', 'kr', 'qh', 'kh', 'vh', 'oh', 'o') to keep allocation out of a timed loop.
+    QK-norm + RoPE -> seq->head of q', k', v -> attention of each of the P
+    head groups (one call per group, as each rank of a P-way group would
+    issue it) -> head->seq of the output.  Returns o [S, H, D].
+
+    fused: norm/RoPE writes q', k' straight into the head-sharded layout
+      (h3attn_qk_norm_rope_seq2head) instead of norm/RoPE then seq2head.
+    attn_chunks: split each group's heads into this many chunks; with an
+      `exchange_stream`, the output exchange of chunk c runs on that stream
+      while attention computes chunk c+1 (the result is bit-identical for any
+      chunk count).  `work` may pass preallocated buffers (make_workspace).
     """
     S, H, D = q.shape
     if work is None:
-        work = make_workspace(S, H, D, P, q.device)
-    qr, kr = work["qr"], work["kr"]
-    h3attn_qk_norm_rope(q, k, qr, kr, w_q, w_k, pos, d_t, d_h, d_w, eps, theta, stream=stream)
-    h3attn_seq2head(qr, work["qh"], P, stream)
-    h3attn_seq2head(kr, work["kh"], P, stream)
+        work = make_workspace(S, H, D, P, q.device, fused=fused)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    if fused:
+        h3attn_qk_norm_rope_seq2head(q, k, work["qh"], work["kh"], w_q, w_k, pos, P, d_t, d_h, d_w, eps, theta,
+                                     stream=stream)
+    else:
+        h3attn_qk_norm_rope(q, k, work["qr"], work["kr"], w_q, w_k, pos, d_t, d_h, d_w, eps, theta, stream=stream)
+        h3attn_seq2head(work["qr"], work["qh"], P, stream)
+        h3attn_seq2head(work["kr"], work["kh"], P, stream)
     h3attn_seq2head(v, work["vh"], P, stream)
+    Hp = H // P
+    if attn_chunks <= 1 and exchange_stream is None:
+        for g in range(P):
+            h3attn_forward(work["qh"][g], work["kh"][g], work["vh"][g], work["oh"][g], kv_len=kv_len, stream=stream)
+        h3attn_head2seq(work["oh"], work["o"], P, stream)
+        return work["o"]
+    xs = exchange_stream if exchange_stream is not None else stream
+    bounds = [round(c * Hp / attn_chunks) for c in range(attn_chunks + 1)]
     for g in range(P):
-        h3attn_forward(work["qh"][g], work["kh"][g], work["vh"][g], work["oh"][g],
-                       kv_len=kv_len, stream=stream)
-    h3attn_head2seq(work["oh"], work["o"], P, stream)
+        for c in range(attn_chunks):
+            j0, j1 = bounds[c], bounds[c + 1]
+            if j1 <= j0:
+                continue
+            h3attn_forward(work["qh"][g], work["kh"][g], work["vh"][g], work["oh"][g], head_begin=j0,
+                           head_count=j1 - j0, kv_len=kv_len, stream=stream)
+            if xs is not stream:
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                xs.wait_event(ev)
+            h3attn_head2seq_heads(work["oh"][g], work["o"], P, g, j0, j1 - j0, stream=xs)
+    if xs is not stream:
+        ev = torch.cuda.Event()
+        ev.record(xs)
+        stream.wait_event(ev)
     return work["o"]
 
 
-def make_workspace(S, H, D, P, device):
+def make_workspace(S, H, D, P, device, fused=True):
     """Buffers for ulysses_attention_step (allocated once by the caller)."""
     e = dict(dtype=torch.bfloat16, device=device)
-    return {"qr": torch.empty((S, H, D), **e), "kr": torch.empty((S, H, D), **e),
-            "qh": torch.empty((P, S, H // P, D), **e), "kh": torch.empty((P, S, H // P, D), **e),
-            "vh": torch.empty((P, S, H // P, D), **e), "oh": torch.empty((P, S, H // P, D), **e),
-            "o": torch.empty((S, H, D), **e)}
+    w = {"qh": torch.empty((P, S, H // P, D), **e), "kh": torch.empty((P, S, H // P, D), **e),
+         "vh": torch.empty((P, S, H // P, D), **e), "oh": torch.empty((P, S, H // P, D), **e),
+         "o": torch.empty((S, H, D), **e)}
+    if not fused:
+        w["qr"] = torch.empty((S, H, D), **e)
+        w["kr"] = torch.empty((S, H, D), **e)
+    return w

@@ -32,10 +32,12 @@ int launch_attention(const void* q, const void* k, const void* v, void* o, int S
 
 int launch_norm_rope(const void* q, const void* k, void* q_out, void* k_out, float* dbg, const float* w_q,
                      const float* w_k, const int32_t* pos, int B, int S, int H, int D, int d_t, int d_h, int d_w,
-                     float eps, double theta, cudaStream_t stream);
+                     float eps, double theta, int P, cudaStream_t stream);
 
 int launch_seq2head(const void* in, void* out, int S, int H, int D, int P, cudaStream_t stream);
 int launch_head2seq(const void* in, void* out, int S, int H, int D, int P, cudaStream_t stream);
+int launch_head2seq_heads(const void* in_group, void* out, int S, int H, int D, int P, int g, int j0, int jc,
+                          cudaStream_t stream);
 
 int launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 

@@ -182,7 +182,31 @@ int h3attn_qk_norm_rope(const void* q, const void* k, void* q_out, void* k_out, 
     int rc = check_device();
     if (rc != H3ATTN_OK) return rc;
     return launch_norm_rope(q, k, q_out, k_out, dbg_fp32, w_q, w_k, pos, B, S, H, D, d_t, d_h, d_w, eps,
-                            static_cast<double>(theta), static_cast<cudaStream_t>(stream));
+                            static_cast<double>(theta), 1, static_cast<cudaStream_t>(stream));
+}
+
+int h3attn_qk_norm_rope_seq2head(const void* q, const void* k, void* qh_out, void* kh_out, float* dbg_fp32,
+                                 const float* w_q, const float* w_k, const int32_t* pos, int S, int H, int D,
+                                 int P, int d_t, int d_h, int d_w, float eps, float theta, void* stream) {
+    if (!q || !k || !qh_out || !kh_out || !w_q || !w_k || !pos) return H3ATTN_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(qh_out) || !aligned16(kh_out) || !aligned16(w_q) ||
+        !aligned16(w_k) || (dbg_fp32 && !aligned16(dbg_fp32)))
+        return H3ATTN_ERR_ARG;
+    if (!(eps >= 0.0f) || !(theta > 0.0f)) return H3ATTN_ERR_ARG;
+    if (S < 1 || H < 1 || P < 1 || (D != 64 && D != 128)) return H3ATTN_ERR_SHAPE;
+    if (S % P != 0 || H % P != 0) return H3ATTN_ERR_SHAPE;
+    if (d_t < 0 || d_h < 0 || d_w < 0 || (d_t | d_h | d_w) & 1 || d_t + d_h + d_w != D) return H3ATTN_ERR_SHAPE;
+    const size_t bytes = static_cast<size_t>(S) * H * D * 2;
+    // the output is a permutation of the input, so it may not share memory with it
+    if (overlap(q, bytes, qh_out, bytes) || overlap(k, bytes, kh_out, bytes) || overlap(q, bytes, kh_out, bytes) ||
+        overlap(k, bytes, qh_out, bytes) || overlap(qh_out, bytes, kh_out, bytes))
+        return H3ATTN_ERR_ALIAS;
+    if (dbg_fp32 && (overlap(dbg_fp32, bytes * 4, qh_out, bytes) || overlap(dbg_fp32, bytes * 4, kh_out, bytes)))
+        return H3ATTN_ERR_ALIAS;
+    int rc = check_device();
+    if (rc != H3ATTN_OK) return rc;
+    return launch_norm_rope(q, k, qh_out, kh_out, dbg_fp32, w_q, w_k, pos, 1, S, H, D, d_t, d_h, d_w, eps,
+                            static_cast<double>(theta), P, static_cast<cudaStream_t>(stream));
 }
 
 int h3attn_forward(const void* q, const void* k, const void* v, void* o, int B, int S, int H_buf, int D,
@@ -226,6 +250,24 @@ int h3attn_head2seq(const void* in, void* out, int S, int H, int D, int P, void*
     if (rc != H3ATTN_OK) return rc;
     if ((rc = check_device()) != H3ATTN_OK) return rc;
     return launch_head2seq(in, out, S, H, D, P, static_cast<cudaStream_t>(stream));
+}
+
+int h3attn_head2seq_heads(const void* in_group, void* out, int S, int H, int D, int P, int group,
+                          int head_begin, int head_count, void* stream) {
+    if (in_group == nullptr || out == nullptr) return H3ATTN_ERR_ARG;
+    if (!aligned16(in_group) || !aligned16(out)) return H3ATTN_ERR_ARG;
+    if (S < 1 || H < 1 || P < 1 || (D != 64 && D != 128) || H % P != 0) return H3ATTN_ERR_SHAPE;
+    const int Hp = H / P;
+    if (group < 0 || group >= P || head_begin < 0 || head_count < 1 || head_begin + head_count > Hp)
+        return H3ATTN_ERR_SHAPE;
+    const uint64_t elems = static_cast<uint64_t>(S) * H * D;
+    if (elems / 8 >= (1ull << 32)) return H3ATTN_ERR_SHAPE;
+    const size_t in_bytes = static_cast<size_t>(S) * Hp * D * 2;
+    if (overlap(in_group, in_bytes, out, elems * 2)) return H3ATTN_ERR_ALIAS;
+    int rc = check_device();
+    if (rc != H3ATTN_OK) return rc;
+    return launch_head2seq_heads(in_group, out, S, H, D, P, group, head_begin, head_count,
+                                 static_cast<cudaStream_t>(stream));
 }
 
 int h3attn_get_device_status(void* stream) {

@@ -74,6 +74,52 @@ __global__ void __launch_bounds__(kLayoutThreads) head2seq_kernel(const uint4* _
     }
 }
 
+// head2seq for a chunk of one group's heads: group g's buffer [S][H/P][D],
+// heads [j0, j0 + jc) -> out[s][g*(H/P) + j].  Used to overlap the output
+// exchange of one head chunk with the attention of the next.
+__global__ void __launch_bounds__(kLayoutThreads) head2seq_heads_kernel(const uint4* __restrict__ in,
+                                                                        uint4* __restrict__ out, uint32_t H,
+                                                                        uint32_t Hp, uint32_t hbase, uint32_t j0,
+                                                                        uint32_t jc, uint32_t vpr_log2,
+                                                                        uint32_t total) {
+    const uint32_t base = blockIdx.x * (kLayoutThreads * kLayoutUnroll) + threadIdx.x;
+    uint4 v[kLayoutUnroll];
+#pragma unroll
+    for (int u = 0; u < kLayoutUnroll; ++u) {
+        const uint32_t i = base + u * kLayoutThreads;
+        if (i < total) {
+            const uint32_t part = i & ((1u << vpr_log2) - 1u);
+            const uint32_t rest = i >> vpr_log2;  // s * jc + jj
+            const uint32_t s = rest / jc, jj = rest - s * jc;
+            v[u] = __ldcs(in + (((s * Hp + j0 + jj) << vpr_log2) + part));
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kLayoutUnroll; ++u) {
+        const uint32_t i = base + u * kLayoutThreads;
+        if (i < total) {
+            const uint32_t part = i & ((1u << vpr_log2) - 1u);
+            const uint32_t rest = i >> vpr_log2;
+            const uint32_t s = rest / jc, jj = rest - s * jc;
+            __stcs(out + (((s * H + hbase + j0 + jj) << vpr_log2) + part), v[u]);
+        }
+    }
+}
+
+int launch_head2seq_heads(const void* in_group, void* out, int S, int H, int D, int P, int g, int j0, int jc,
+                          cudaStream_t stream) {
+    const uint32_t vpr_log2 = (D == 128) ? 4u : 3u;
+    const uint64_t total64 = static_cast<uint64_t>(S) * jc * (static_cast<uint64_t>(D) / 8);
+    if (total64 == 0) return H3ATTN_OK;
+    const uint32_t total = static_cast<uint32_t>(total64);
+    const uint32_t per_block = kLayoutThreads * kLayoutUnroll;
+    const uint32_t Hp = static_cast<uint32_t>(H / P);
+    head2seq_heads_kernel<<<(total + per_block - 1) / per_block, kLayoutThreads, 0, stream>>>(
+        static_cast<const uint4*>(in_group), static_cast<uint4*>(out), H, Hp, g * Hp, j0, jc, vpr_log2, total);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e);
+}
+
 static int launch_layout(bool to_heads, const void* in, void* out, int S, int H, int D, int P,
                          cudaStream_t stream) {
     const uint32_t vpr_log2 = (D == 128) ? 4u : 3u;  // 16-byte vectors per head row

@@ -6,16 +6,22 @@
 // is inv_freq times the position.  Per (token, head) row of q and of k:
 //     y = x / sqrt(mean(x^2) + eps) * w;   pair i of axis a rotated by pos_a * theta^(-2i/d_a).
 //
-// One block per token.  The token's D/2 rotation angles are shared by all
+// One block of 128 threads per token.  The token's D/2 rotation angles are shared by all
 // 2*H rows (q and k, every head), so the block computes cos/sin once: the
 // angle pos * inv_freq and its reduction to [-pi, pi] in fp64 (a handful of
 // fp64 ops per pair; the position is an exact integer, so the reduced angle
 // is accurate to ~1e-16 even for positions in the thousands), then sincosf on
 // the reduced fp32 angle.  Each thread owns 8 consecutive dims (one 16-byte
 // vector) of a row, i.e. 4 whole rotation pairs; the D/8 threads of a row
-// reduce the sum of squares with warp shuffles.  All loads of the token are
-// issued before any is used (up to 8 vectors per thread in flight).
+// reduce the sum of squares with warp shuffles.  Loads are issued four
+// vectors per thread at a time, the first batch before the angle work;
+// results leave with streaming (evict-first) stores.  Small blocks and few
+// registers keep many tokens in flight per SM.
 // HBM-bound: 4 * H * D * 2 bytes per token (read and write q and k).
+//
+// With P > 1 the results are written straight into the Ulysses head-sharded
+// layout [P][S][H/P][D] (the layout seq2head produces), so the normalised q
+// and k never make a token-major round trip through HBM before the exchange.
 #include <cmath>
 #include <cstdint>
 
@@ -24,8 +30,8 @@
 
 namespace h3 {
 
-constexpr int kNormThreads = 256;
-constexpr int kNormMaxVec = 8;  // vectors per thread held in registers per pass
+constexpr int kNormThreads = 128;
+constexpr int kNormMaxVec = 4;  // vectors per thread held in registers per pass
 
 struct RopeTable {
     double inv_freq[64];   // per rotation pair p = (global dim)/2
@@ -36,7 +42,7 @@ template <int D>
 __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
     const uint4* q, const uint4* k, uint4* qo, uint4* ko, float* __restrict__ dbg,
     const float* __restrict__ wq, const float* __restrict__ wk, const int32_t* __restrict__ pos, int S, int H,
-    float eps, size_t dbg_k_offset, const RopeTable tab) {
+    float eps, size_t dbg_k_offset, int P, const RopeTable tab) {
     constexpr int VPR = D / 8;  // vectors per row
     constexpr double kTwoPi = 6.283185307179586476925286766559;
     constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
@@ -44,6 +50,25 @@ __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
 
     const int tok = blockIdx.x;  // b * S + s
     const int s = tok % S;
+    const int cpt = H * VPR;      // vectors per tensor for this token
+    const int total = 2 * cpt;
+    const int iters = (total + kNormThreads - 1) / kNormThreads;
+    const size_t tok_vec = static_cast<size_t>(tok) * cpt;
+    const float inv_d = 1.0f / static_cast<float>(D);
+
+    // Issue the first batch of q/k loads before anything else, so their
+    // latency overlaps the position load and the angle computation below.
+    uint4 x[kNormMaxVec];
+#pragma unroll
+    for (int u = 0; u < kNormMaxVec; ++u) {
+        const int idx = u * kNormThreads + threadIdx.x;
+        if (u < iters && idx < total) {
+            const bool is_k = idx >= cpt;
+            x[u] = __ldcs((is_k ? k : q) + tok_vec + (is_k ? idx - cpt : idx));
+        } else {
+            x[u] = make_uint4(0, 0, 0, 0);
+        }
+    }
     if (threadIdx.x < D / 2) {
         const int pr = threadIdx.x;
         const double ang = static_cast<double>(__ldg(pos + 3 * s + tab.axis[pr])) * tab.inv_freq[pr];
@@ -55,23 +80,17 @@ __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
     }
     __syncthreads();
 
-    const int cpt = H * VPR;      // vectors per tensor for this token
-    const int total = 2 * cpt;
-    const int iters = (total + kNormThreads - 1) / kNormThreads;
-    const size_t tok_vec = static_cast<size_t>(tok) * cpt;
-    const float inv_d = 1.0f / static_cast<float>(D);
-
     for (int it0 = 0; it0 < iters; it0 += kNormMaxVec) {
-        uint4 x[kNormMaxVec];
+        if (it0 > 0) {
 #pragma unroll
-        for (int u = 0; u < kNormMaxVec; ++u) {
-            const int idx = (it0 + u) * kNormThreads + threadIdx.x;
-            if (it0 + u < iters && idx < total) {
-                const bool is_k = idx >= cpt;
-                const int c = is_k ? idx - cpt : idx;
-                x[u] = __ldcs((is_k ? k : q) + tok_vec + c);
-            } else {
-                x[u] = make_uint4(0, 0, 0, 0);
+            for (int u = 0; u < kNormMaxVec; ++u) {
+                const int idx = (it0 + u) * kNormThreads + threadIdx.x;
+                if (it0 + u < iters && idx < total) {
+                    const bool is_k = idx >= cpt;
+                    x[u] = __ldcs((is_k ? k : q) + tok_vec + (is_k ? idx - cpt : idx));
+                } else {
+                    x[u] = make_uint4(0, 0, 0, 0);
+                }
             }
         }
 #pragma unroll
@@ -114,7 +133,14 @@ __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
             out.y = pack_bf16x2(y[2], y[3]);
             out.z = pack_bf16x2(y[4], y[5]);
             out.w = pack_bf16x2(y[6], y[7]);
-            (is_k ? ko : qo)[tok_vec + c] = out;
+            size_t dst = tok_vec + c;
+            if (P > 1) {  // head-sharded output: [g][s][j] with h = g * (H/P) + j (one batch item)
+                const int Hp = H / P;
+                const int h = c / VPR;
+                const int g = h / Hp;
+                dst = ((static_cast<size_t>(g) * S + s) * Hp + (h - g * Hp)) * VPR + part;
+            }
+            __stcs((is_k ? ko : qo) + dst, out);
             if (dbg != nullptr) {
                 float4* d4 = reinterpret_cast<float4*>(dbg + (is_k ? dbg_k_offset : 0) + (tok_vec + c) * 8);
                 d4[0] = make_float4(y[0], y[1], y[2], y[3]);
@@ -126,7 +152,7 @@ __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
 
 int launch_norm_rope(const void* q, const void* k, void* q_out, void* k_out, float* dbg, const float* w_q,
                      const float* w_k, const int32_t* pos, int B, int S, int H, int D, int d_t, int d_h, int d_w,
-                     float eps, double theta, cudaStream_t stream) {
+                     float eps, double theta, int P, cudaStream_t stream) {
     RopeTable tab;
     const int width[3] = {d_t, d_h, d_w};
     int pr = 0;
@@ -146,11 +172,11 @@ int launch_norm_rope(const void* q, const void* k, void* q_out, void* k_out, flo
     if (D == 128)
         norm_rope_kernel<128><<<blocks, kNormThreads, 0, stream>>>(
             static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<uint4*>(q_out),
-            static_cast<uint4*>(k_out), dbg, w_q, w_k, pos, S, H, eps, dbg_k, tab);
+            static_cast<uint4*>(k_out), dbg, w_q, w_k, pos, S, H, eps, dbg_k, P, tab);
     else
         norm_rope_kernel<64><<<blocks, kNormThreads, 0, stream>>>(
             static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<uint4*>(q_out),
-            static_cast<uint4*>(k_out), dbg, w_q, w_k, pos, S, H, eps, dbg_k, tab);
+            static_cast<uint4*>(k_out), dbg, w_q, w_k, pos, S, H, eps, dbg_k, P, tab);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e);
 }

@@ -78,6 +78,24 @@ H3ATTN_API int h3attn_qk_norm_rope(const void* q, const void* k, void* q_out, vo
                         int d_t, int d_h, int d_w, float eps, float theta, void* stream);
 
 /*
+ * h3attn_qk_norm_rope_seq2head -- h3attn_qk_norm_rope followed by
+ * h3attn_seq2head of its q and k outputs, in one pass: the results are
+ * written straight into the Ulysses head-sharded layout.  The README of
+ * "buqi-minimax-h3-multigpu" ("How it works") counts the transpose+copy steps
+ * around the exchange as a cost worth removing; here the normalised q and k
+ * skip their token-major round trip through HBM.
+ *   q, k          [S][H][D] bf16 (one batch item; the P sequence shards).
+ *   qh_out,kh_out [P][S][H/P][D] bf16, bit-identical to
+ *                 seq2head(qk_norm_rope(q, k)); must not overlap q or k.
+ *   dbg_fp32      NULL, or [2][S][H][D] fp32 (token-major, unrounded q then k).
+ *   S % P == 0, H % P == 0; other arguments as h3attn_qk_norm_rope.
+ */
+H3ATTN_API int h3attn_qk_norm_rope_seq2head(const void* q, const void* k, void* qh_out, void* kh_out,
+                                            float* dbg_fp32, const float* w_q, const float* w_k,
+                                            const int32_t* pos, int S, int H, int D, int P, int d_t, int d_h,
+                                            int d_w, float eps, float theta, void* stream);
+
+/*
  * h3attn_forward -- exact softmax attention for a range of heads.
  *
  * Defined by "buqi-minimax-h3-multigpu" README, sections "On accuracy" and
@@ -122,6 +140,20 @@ H3ATTN_API int h3attn_seq2head(const void* in, void* out, int S, int H, int D, i
  * head2seq(seq2head(x)) == x bit for bit.  in and out must not overlap.
  */
 H3ATTN_API int h3attn_head2seq(const void* in, void* out, int S, int H, int D, int P, void* stream);
+
+/*
+ * h3attn_head2seq_heads -- the output exchange for one chunk of one group's
+ * heads, so that it can run on a second stream while attention computes the
+ * next chunk ("buqi-minimax-h3-multigpu" README, "How it works": attention
+ * runs in head chunks and each chunk's output exchange overlaps the next
+ * chunk's compute; the result does not depend on the chunk count).
+ *   in_group  [S][H/P][D] bf16: head group `group` (0 <= group < P).
+ *   out       [S][H][D] bf16; heads group*(H/P) + j for j in
+ *             [head_begin, head_begin + head_count) are written, no others.
+ *   in_group and out must not overlap.
+ */
+H3ATTN_API int h3attn_head2seq_heads(const void* in_group, void* out, int S, int H, int D, int P, int group,
+                                     int head_begin, int head_count, void* stream);
 
 /*
  * h3attn_get_device_status -- synchronise `stream`, then read and clear the

@@ -82,6 +82,17 @@ def test_argument_checks_run_before_any_cuda_call(lib):
     assert f(*args, 16, 24, 24, -1.0, 1e4, null) == h3.H3ATTN_ERR_ARG
     assert f(*args, 16, 24, 24, 1e-6, 0.0, null) == h3.H3ATTN_ERR_ARG
     assert lib.h3attn_selftest_wait_timeout(0, null) == h3.H3ATTN_ERR_ARG
+    g = lib.h3attn_qk_norm_rope_seq2head
+    base = [fake, fake + 0x100000, fake + 0x200000, fake + 0x300000, null, fake + 0x400000, fake + 0x500000,
+            fake + 0x600000]
+    assert g(*base, 64, 56, 128, 3, 32, 48, 48, 1e-6, 1e4, null) == h3.H3ATTN_ERR_SHAPE      # P does not divide H
+    assert g(*base, 64, 56, 128, 2, 32, 48, 46, 1e-6, 1e4, null) == h3.H3ATTN_ERR_SHAPE      # split != D
+    assert g(fake, fake + 0x100000, fake + 0x10, fake + 0x300000, null, fake + 0x400000, fake + 0x500000,
+             fake + 0x600000, 64, 56, 128, 2, 32, 48, 48, 1e-6, 1e4, null) == h3.H3ATTN_ERR_ALIAS  # out overlaps q
+    f2 = lib.h3attn_head2seq_heads
+    assert f2(fake, fake + 0x1000000, 64, 56, 128, 2, 2, 0, 1, null) == h3.H3ATTN_ERR_SHAPE   # group >= P
+    assert f2(fake, fake + 0x1000000, 64, 56, 128, 2, 1, 20, 9, null) == h3.H3ATTN_ERR_SHAPE  # past H/P
+    assert f2(fake, fake + 0x100, 64, 56, 128, 2, 1, 0, 4, null) == h3.H3ATTN_ERR_ALIAS
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -234,3 +234,72 @@ def test_device_timeout_is_reported_and_context_survives(h3, cuda_device):
     assert h3.h3attn_get_device_status() == 0  # cleared
     x = torch.ones(1024, device=cuda_device)
     assert float(x.sum()) == 1024.0
+
+
+# ------------------------------------------- fused norm/RoPE + seq->head
+@pytest.mark.parametrize("name,P", [("tiny", 1), ("tiny", 4), ("c2", 2), ("c2", 7), ("c2", 8)])
+def test_fused_norm_rope_seq2head(h3, cuda_device, name, P):
+    w = synth.WORKLOADS[name]
+    S = w.S if w.S % P == 0 else (w.S // P) * P
+    dev = cuda_device
+    shape = (S, w.H, w.D)
+    q, k = synth.randn_bf16(shape, synth.SEED_Q), synth.randn_bf16(shape, synth.SEED_K)
+    wq, wk = synth.norm_weights(w.D)
+    pos = synth.packed_positions(w)[:S]
+    qd, kd, wqd, wkd, posd = q.to(dev), k.to(dev), wq.to(dev), wk.to(dev), torch.from_numpy(pos).to(dev)
+    hs = (P, S, w.H // P, w.D)
+    qh, kh = torch.empty(hs, dtype=torch.bfloat16, device=dev), torch.empty(hs, dtype=torch.bfloat16, device=dev)
+    dbg = torch.empty((2,) + shape, dtype=torch.float32, device=dev)
+    h3.h3attn_qk_norm_rope_seq2head(qd, kd, qh, kh, wqd, wkd, posd, P, *w.rope_split, w.eps, w.theta, dbg_fp32=dbg)
+    # bit-identical to the two-pass path (norm/RoPE token-major, then the exchange)
+    qr, kr = torch.empty_like(qd), torch.empty_like(kd)
+    h3.h3attn_qk_norm_rope(qd, kd, qr, kr, wqd, wkd, posd, *w.rope_split, w.eps, w.theta)
+    qh2, kh2 = torch.empty_like(qh), torch.empty_like(kh)
+    h3.h3attn_seq2head(qr, qh2, P)
+    h3.h3attn_seq2head(kr, kh2, P)
+    assert h3.h3attn_get_device_status() == 0
+    assert torch.equal(qh.view(torch.int16), qh2.view(torch.int16))
+    assert torch.equal(kh.view(torch.int16), kh2.view(torch.int16))
+    # and within one bf16 ulp (+ the fp32 bound) of the oracle in the head-sharded layout
+    for t, src, wt in ((qh, q, wq), (kh, k, wk)):
+        ref = oracle.norm_rope(oracle.bf16_to_f64(src), wt.double().numpy(), pos, w.eps, *w.rope_split, w.theta)
+        ref = ref.reshape(S, P, w.H // P, w.D).transpose(1, 0, 2, 3)
+        got = t.double().cpu().numpy()
+        ref_b = torch.from_numpy(np.ascontiguousarray(ref)).to(torch.bfloat16).double().numpy()
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref_b), 2.0 ** -126))) - 7)
+        assert np.all(np.abs(got - ref) <= ulp + NORM_TOL * np.abs(ref).max())
+
+
+# ------------------------------------------- head-chunked output exchange
+def test_chunked_step_bit_identical_for_any_chunk_count(h3, cuda_device):
+    w = synth.WORKLOADS["c2"]
+    dev = cuda_device
+    q, k, v = synth.qkv(w, dev)
+    wq, wk = (t.to(dev) for t in synth.norm_weights(w.D))
+    pos = torch.from_numpy(synth.packed_positions(w)).to(dev)
+    args = (q, k, v, wq, wk, pos, 2, w.S_v, *w.rope_split, w.eps, w.theta)
+    ref = h3.ulysses_attention_step(*args, fused=False).clone()
+    side = torch.cuda.Stream(dev)
+    for fused in (True, False):
+        for chunks in (1, 2, 4, 8):
+            for xs in (None, side):
+                o = h3.ulysses_attention_step(*args, fused=fused, attn_chunks=chunks, exchange_stream=xs)
+                torch.cuda.synchronize()
+                assert torch.equal(o.view(torch.int16), ref.view(torch.int16)), (fused, chunks, xs)
+    assert h3.h3attn_get_device_status() == 0
+
+
+def test_head2seq_heads_writes_only_its_heads(h3, cuda_device):
+    S, H, D, P = 300, 56, 128, 4
+    dev = cuda_device
+    x = synth.randn_bf16((S, H, D), 81, dev)
+    groups = torch.empty((P, S, H // P, D), dtype=torch.bfloat16, device=dev)
+    h3.h3attn_seq2head(x, groups, P)
+    out = torch.full((S, H, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    h3.h3attn_head2seq_heads(groups[2], out, P, 2, 3, 5)
+    torch.cuda.synchronize()
+    sel = slice(2 * (H // P) + 3, 2 * (H // P) + 8)
+    assert torch.equal(out[:, sel].view(torch.int16), x[:, sel].view(torch.int16))
+    mask = torch.ones(H, dtype=torch.bool)
+    mask[sel] = False
+    assert torch.isnan(out[:, mask].float()).all()
