@@ -126,3 +126,17 @@ def qkv(w: Workload, device="cpu", zero_pad=True):
     return (randn_bf16(shape, SEED_Q, device, z),
             randn_bf16(shape, SEED_K, device, z),
             randn_bf16(shape, SEED_V, device, z))
+
+
+# Hidden / projection sizes of the H3 block: hidden 5376, attention inner width
+# 7168 = 56 heads x 128 ("buqi-minimax-h3-multigpu" README, "How it works").
+HIDDEN, INNER = 5376, 7168
+
+
+def fp8_e4m3_codes(shape, seed: int, std: float, device="cpu") -> torch.Tensor:
+    """Seeded N(0, std^2) draws rounded to FP8 E4M3, returned as raw uint8 codes."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    t = torch.randn(shape, generator=g, dtype=torch.float32, device=dev) * std
+    return t.to(torch.float8_e4m3fn).view(torch.uint8)

@@ -44,6 +44,10 @@ def _load():
         lib.h3o_attention.argtypes = [p, i64, p, p, i64, i32, i32, i64, d, p]
         lib.h3o_seq2head_u16.argtypes = [p, p, i64, i32, i32, i32]
         lib.h3o_head2seq_u16.argtypes = [p, p, i64, i32, i32, i32]
+        lib.h3o_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.h3o_e4m3_decode.restype = d
+        lib.h3o_qkv_proj_fp8.argtypes = [p, i64, p, i32, i32, i32, i32, d, p]
+        lib.h3o_qkv_proj_fp8.restype = None
         lib.h3o_num_threads.restype = i32
         for f in (lib.h3o_rmsnorm, lib.h3o_rope, lib.h3o_attention,
                   lib.h3o_seq2head_u16, lib.h3o_head2seq_u16):
@@ -123,6 +127,24 @@ def head2seq(x_u16, P: int) -> np.ndarray:
     assert P_ == P and S % P == 0
     out = np.empty((S, Hp * P, D), dtype=np.uint16)
     _load().h3o_head2seq_u16(_ptr(x), _ptr(out), S, Hp * P, D, P)
+    return out
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one FP8 E4M3 code (NaN for S.1111.111)."""
+    return float(_load().h3o_e4m3_decode(int(code) & 0xFF))
+
+
+def qkv_proj_fp8(x_codes, w_codes, scale: float, inner: int, P: int, rank: int) -> np.ndarray:
+    """Projection of the given rows of x ([n, hidden] E4M3 codes) through rank
+    `rank`'s head rows of w ([3*inner, hidden] E4M3 codes), times `scale`.
+    Returns [n, 3, inner/P] float64 (q, k, v parts)."""
+    x = np.ascontiguousarray(x_codes, dtype=np.uint8)
+    w = np.ascontiguousarray(w_codes, dtype=np.uint8)
+    n, hidden = x.shape
+    assert w.shape == (3 * inner, hidden) and inner % P == 0 and 0 <= rank < P
+    out = np.empty((n, 3, inner // P), dtype=np.float64)
+    _load().h3o_qkv_proj_fp8(_ptr(x), n, _ptr(w), hidden, inner, P, rank, float(scale), _ptr(out))
     return out
 
 

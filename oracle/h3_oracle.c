@@ -202,3 +202,59 @@ void h3o_head2seq_u16(const uint16_t *in, uint16_t *out, int64_t S, int H,
         }
     }
 }
+
+/* ---------------------------------------------------------------------------
+ * All-gather exchange variant: the QKV projection through one rank's head
+ * rows ("buqi-minimax-h3-multigpu" README, "How it works": for world sizes up
+ * to 4 each rank receives the full modulated hidden state and multiplies it by
+ * only its own head rows of qkv_proj; slicing the fp8 weight by rows is exact
+ * because its scale is one number per tensor).
+ *
+ * Readings: qkv_proj is a Linear of shape [3*inner, hidden] stored row-major
+ * (q rows, then k rows, then v rows; inside each, head h owns rows
+ * [h*D, (h+1)*D)); rank r of P owns rows [part*inner + r*inner/P,
+ * part*inner + (r+1)*inner/P) of each part; both operands are FP8 E4M3
+ * (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,
+ * S.1111.111 is NaN) with one scale per tensor; no bias term.
+ * ------------------------------------------------------------------------- */
+
+/* FP8 E4M3 code -> value, written from the format's definition. */
+double h3o_e4m3_decode(uint8_t code)
+{
+    const int sign = (code >> 7) & 1;
+    const int e = (code >> 3) & 0xF;
+    const int m = code & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);          /* subnormal: 0.m * 2^(1-7) */
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);  /* normal: 1.m * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* out[r][part][c] = scale * sum_e x[r][e] * w[part*inner + rank*inner/P + c][e]
+ * for the n_rows given rows of x ([n_rows][hidden] codes), part in {q,k,v},
+ * c in [0, inner/P).  out is [n_rows][3][inner/P] doubles.                  */
+void h3o_qkv_proj_fp8(const uint8_t *x, int64_t n_rows, const uint8_t *w, int hidden, int inner, int P,
+                      int rank, double scale, double *out)
+{
+    const int nr = inner / P;
+    double table[256];
+    for (int c = 0; c < 256; ++c)
+        table[c] = h3o_e4m3_decode((uint8_t)c);
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        for (int part = 0; part < 3; ++part) {
+            const uint8_t *xr = x + r * hidden;
+            for (int c = 0; c < nr; ++c) {
+                const uint8_t *wr = w + ((int64_t)part * inner + (int64_t)rank * nr + c) * hidden;
+                double acc = 0.0;
+                for (int e = 0; e < hidden; ++e)
+                    acc += table[xr[e]] * table[wr[e]];
+                out[(r * 3 + part) * (int64_t)nr + c] = scale * acc;
+            }
+        }
+    }
+}

@@ -258,3 +258,58 @@ def test_seeded_inputs_are_reproducible():
     assert torch.equal(a, b) and a.dtype == torch.bfloat16
     wq, wk = synth.norm_weights(64)
     assert wq.shape == (64,) and not torch.equal(wq, wk)
+
+
+# ------------------------------------------------- fp8 QKV projection (all-gather variant)
+def test_e4m3_decode_golden():
+    import os
+    from conftest import GOLDEN
+    for line in open(os.path.join(GOLDEN, "e4m3_decode.txt")):
+        line = line.split("#", 1)[0].split()
+        if len(line) == 2:
+            assert oracle.e4m3_decode(int(line[0], 16)) == float(line[1]), line
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+
+
+def test_e4m3_decode_matches_torch_float8_for_all_codes():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+
+
+def _fp8_codes(shape, seed, std):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * std).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_qkv_proj_matches_numpy_matmul_of_decoded_values():
+    n, hidden, inner = 5, 96, 32
+    x, w = _fp8_codes((n, hidden), 1, 1.0), _fp8_codes((3 * inner, hidden), 2, 4.0)
+    table = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    ref = (table[x] @ table[w].T) * 0.125
+    got = oracle.qkv_proj_fp8(x, w, 0.125, inner, 1, 0)
+    np.testing.assert_allclose(got.reshape(n, 3 * inner), ref, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("P", [2, 4, 7, 8])
+def test_qkv_proj_rank_slices_are_the_columns_of_the_full_projection(P):
+    n, hidden, inner = 3, 64, 56
+    x, w = _fp8_codes((n, hidden), 3, 1.0), _fp8_codes((3 * inner, hidden), 4, 2.0)
+    full = oracle.qkv_proj_fp8(x, w, 0.5, inner, 1, 0)          # [n, 3, inner]
+    parts = np.concatenate([oracle.qkv_proj_fp8(x, w, 0.5, inner, P, r) for r in range(P)], axis=2)
+    np.testing.assert_array_equal(parts, full)
+
+
+def test_qkv_proj_brute_force_python_loops():
+    n, hidden, inner, P, rank = 2, 8, 4, 2, 1
+    x, w = _fp8_codes((n, hidden), 5, 1.0), _fp8_codes((3 * inner, hidden), 6, 1.0)
+    got = oracle.qkv_proj_fp8(x, w, 2.0, inner, P, rank)
+    for r in range(n):
+        for part in range(3):
+            for c in range(inner // P):
+                row = part * inner + rank * (inner // P) + c
+                ref = 2.0 * sum(oracle.e4m3_decode(x[r, e]) * oracle.e4m3_decode(w[row, e]) for e in range(hidden))
+                assert got[r, part, c] == pytest.approx(ref, rel=1e-14, abs=1e-14)
