@@ -54,6 +54,7 @@ def parse_args():
     ap.add_argument("--P", type=int, default=2, help="Ulysses degree emulated inside one step")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-proj", action="store_true", help="skip timing the all-gather variant's fp8 projection")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
 
@@ -434,6 +435,34 @@ def main():
     h2d = 3 * tensor_bytes + hpos.numel() * 4
     d2h = tensor_bytes
 
+    # ---------------------------------------------- all-gather variant projection
+    proj = None
+    if not args.no_proj and D == 128:
+        hidden, inner = synth.HIDDEN, synth.INNER
+        xg = synth.fp8_e4m3_codes((S, hidden), 41 + rank, 1.0, dev)
+        wg = synth.fp8_e4m3_codes((3 * inner, hidden), 42, 4.0, dev)
+        outs = [torch.empty((S, inner // P), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+        sc = 1.0 / (4.0 * hidden ** 0.5)
+        for _ in range(3):
+            h3.h3attn_qkv_proj_fp8(xg, wg, sc, *outs, P, 0)
+        torch.cuda.synchronize(dev)
+        pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        pa.record(stream)
+        for _ in range(reps):
+            h3.h3attn_qkv_proj_fp8(xg, wg, sc, *outs, P, 0)
+        pb.record(stream)
+        torch.cuda.synchronize(dev)
+        if h3.h3attn_get_device_status() != 0:
+            raise RuntimeError("device status error in the projection timing")
+        pms = pa.elapsed_time(pb) / reps
+        pfl = 2.0 * S * (3 * inner // P) * hidden
+        fp8_peak = 2.0 * peaks["bf16_tflops"]
+        proj = {"kernel": "qkv_proj_fp8_kernel (one rank of P)", "shape": f"[{S} x {hidden}] x [{hidden} x 3*{inner}/{P}]",
+                "ms": pms, "TFLOP_per_s": pfl / (pms * 1e-3) / 1e12,
+                "peak": fp8_peak, "peak_source": f"{peak_src} bf16 burst x 2 (dense fp8 / bf16 nominal ratio)",
+                "frac": pfl / (pms * 1e-3) / 1e12 / fp8_peak}
+        del xg, wg, outs
     if rank != 0:
         return
     cpu = None
@@ -462,6 +491,7 @@ def main():
         "gpu_launches": args.steps * (1 + 1 + P + 1),
         "clocks": clk,
         "cpu_baseline": cpu,
+        "ag_qkv_proj_fp8": proj,
     }
     print(json.dumps(line), flush=True)
 

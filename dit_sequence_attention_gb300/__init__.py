@@ -16,7 +16,7 @@ import torch
 __all__ = [
     "H3AttnError", "load_library", "library_path",
     "h3attn_qk_norm_rope", "h3attn_qk_norm_rope_seq2head", "h3attn_forward", "h3attn_seq2head",
-    "h3attn_head2seq", "h3attn_head2seq_heads",
+    "h3attn_head2seq", "h3attn_head2seq_heads", "h3attn_qkv_proj_fp8",
     "h3attn_get_device_status", "h3attn_strerror", "h3attn_version", "h3attn_selftest_wait_timeout",
     "h3attn_last_device_error_info",
     "ulysses_attention_step",
@@ -41,6 +41,7 @@ SIGNATURES = {
     "h3attn_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
     "h3attn_qk_norm_rope_seq2head": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P]),
     "h3attn_head2seq_heads": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "h3attn_qkv_proj_fp8": (_I, [_P, _P, _F, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "h3attn_seq2head": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "h3attn_head2seq": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "h3attn_get_device_status": (_I, [_P]),
@@ -237,6 +238,30 @@ def h3attn_head2seq_heads(x_group, out, P, group, head_begin, head_count, stream
     rc = lib.h3attn_head2seq_heads(x_group.data_ptr(), out.data_ptr(), S, Hp * P, D, int(P), int(group),
                                    int(head_begin), int(head_count), _stream_ptr(stream))
     _check("h3attn_head2seq_heads", rc)
+
+
+def h3attn_qkv_proj_fp8(x_fp8, w_fp8, scale, q_out, k_out, v_out, P, rank, stream=None):
+    """This rank's q, k, v ([S, inner/P] bf16 each) = scale * x_fp8 [S, hidden] @ its head rows of w_fp8.
+
+    x_fp8 / w_fp8: uint8 tensors of FP8 E4M3 codes (or torch.float8_e4m3fn), w_fp8 [3*inner, hidden].
+    """
+    lib = load_library()
+    for t, n in ((x_fp8, "x_fp8"), (w_fp8, "w_fp8")):
+        if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)) or not t.is_cuda \
+                or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError(f"{n} must be a contiguous 2-D CUDA tensor of E4M3 codes")
+    S, hidden = x_fp8.shape
+    if w_fp8.shape[1] != hidden or w_fp8.shape[0] % 3:
+        raise ValueError("w_fp8 must be [3*inner, hidden]")
+    inner = w_fp8.shape[0] // 3
+    for t, n in ((q_out, "q_out"), (k_out, "k_out"), (v_out, "v_out")):
+        _bf16(t, n, x_fp8.device)
+        if t.numel() != S * (inner // P):
+            raise ValueError(f"{n} must hold S * inner/P = {S * (inner // P)} elements")
+    rc = lib.h3attn_qkv_proj_fp8(x_fp8.data_ptr(), w_fp8.data_ptr(), float(scale), q_out.data_ptr(),
+                                 k_out.data_ptr(), v_out.data_ptr(), S, hidden, inner, int(P), int(rank),
+                                 _stream_ptr(stream))
+    _check("h3attn_qkv_proj_fp8", rc)
 
 
 def h3attn_get_device_status(stream=None) -> int:

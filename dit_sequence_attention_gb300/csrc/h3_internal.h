@@ -39,6 +39,9 @@ int launch_head2seq(const void* in, void* out, int S, int H, int D, int P, cudaS
 int launch_head2seq_heads(const void* in_group, void* out, int S, int H, int D, int P, int g, int j0, int jc,
                           cudaStream_t stream);
 
+int launch_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, void* k_out, void* v_out, int S,
+                        int hidden, int inner, int P, int rank, cudaStream_t stream);
+
 int launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 
 }  // namespace h3

@@ -270,6 +270,28 @@ int h3attn_head2seq_heads(const void* in_group, void* out, int S, int H, int D, 
                                  static_cast<cudaStream_t>(stream));
 }
 
+int h3attn_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, void* k_out, void* v_out, int S,
+                        int hidden, int inner, int P, int rank, void* stream) {
+    if (!x || !w || !q_out || !k_out || !v_out) return H3ATTN_ERR_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(v_out))
+        return H3ATTN_ERR_ARG;
+    if (!(scale == scale)) return H3ATTN_ERR_ARG;
+    if (S < 1 || hidden < 16 || hidden % 16 != 0 || inner < 1 || P < 1 || inner % P != 0) return H3ATTN_ERR_SHAPE;
+    if (rank < 0 || rank >= P || (inner / P) % 8 != 0) return H3ATTN_ERR_SHAPE;
+    const size_t xb = static_cast<size_t>(S) * hidden, wb = static_cast<size_t>(3) * inner * hidden;
+    const size_t ob = static_cast<size_t>(S) * (inner / P) * 2;
+    const void* outs[3] = {q_out, k_out, v_out};
+    for (int i = 0; i < 3; ++i) {
+        if (overlap(outs[i], ob, x, xb) || overlap(outs[i], ob, w, wb)) return H3ATTN_ERR_ALIAS;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlap(outs[i], ob, outs[j], ob)) return H3ATTN_ERR_ALIAS;
+    }
+    int rc = check_device();
+    if (rc != H3ATTN_OK) return rc;
+    return launch_qkv_proj_fp8(x, w, scale, q_out, k_out, v_out, S, hidden, inner, P, rank,
+                               static_cast<cudaStream_t>(stream));
+}
+
 int h3attn_get_device_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);

@@ -1,0 +1,264 @@
+// qkv_proj.cu -- the all-gather exchange variant's QKV projection on sm_103a
+// tensor cores (FP8 E4M3 x E4M3 -> fp32, tcgen05.mma kind::f8f6f4).
+//
+// "buqi-minimax-h3-multigpu" README, "How it works": for world sizes up to 4
+// every rank receives the whole modulated hidden state and multiplies it by
+// only its own head rows of qkv_proj; slicing the fp8 weight by rows is exact
+// because its scale is one number per tensor.  For rank r of P:
+//     out_part[s][c] = scale * sum_e x[s][e] * w[part*inner + r*inner/P + c][e]
+// for part in (q, k, v) and c < inner/P, written as bf16 [S][inner/P] per part
+// (the head-sharded [S][H/P][D] layout the attention kernel reads).
+//
+// One CTA = 128 tokens x 256 output features of one part, 192 threads:
+//   warp 0      TMA producer: x and w tiles of 128 bytes along K into a
+//               4-stage ring (128B swizzle).
+//   warp 1      allocates 256 TMEM columns; one lane issues 4 MMAs (K = 32)
+//               per stage with descriptors built once (start address offsets).
+//   warps 2-5   epilogue: TMEM -> registers, times scale, bf16, global stores.
+// The grid walks the output-feature tiles fastest, so the CTAs that run at the
+// same time share their x rows through L2; the weight slice (58 MB at P = 2)
+// stays L2-resident.  Each output element's K accumulation order is the same
+// whatever the rank or tile, so the per-rank projections are bit-identical to
+// the matching columns of the full (P = 1) projection.
+#include <cuda.h>
+
+#include "h3_device.cuh"
+#include "h3_internal.h"
+
+namespace h3 {
+
+constexpr int kProjThreads = 192;
+
+struct ProjTraits {
+    static constexpr int BM = 128;   // tokens per tile (TMEM lanes)
+    static constexpr int BN = 256;   // output features per tile
+    static constexpr int BK = 128;   // bytes (= E4M3 elements) per stage along K
+    static constexpr int STAGES = 4;
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = STAGES * A_BYTES;
+    static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+    static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+    // kind::f8f6f4: D = f32 (bit 4), A = B = E4M3 (format 0), K-major, N >> 3, M >> 4
+    static constexpr uint32_t IDESC =
+        (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+    static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+};
+
+enum : int { PB_FULL = 0, PB_EMPTY = 4, PB_ACC = 8, PB_DRAIN = 9, PB_COUNT = 10 };
+
+struct ProjParams {
+    __nv_bfloat16* out[3];  // q, k, v: [S][Nr] bf16
+    int S;
+    int Nr;                 // inner / P: output features per part for this rank
+    int wrow0;              // rank * Nr
+    int inner;
+    int n_kblocks;
+    int tiles_per_part;
+    float scale;
+    unsigned long long wait_limit_ns;
+    DeviceStatus* status;
+};
+
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const void* tmap, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void proj_drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > limit_ns) break;
+    }
+}
+
+__global__ void __launch_bounds__(kProjThreads, 1)
+    qkv_proj_fp8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                        const ProjParams p) {
+    using T = ProjTraits;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - raw);
+    const uint32_t bar0 = sbase + T::OFF_BAR;
+    auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::OFF_BAR + 8 * PB_COUNT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_BAR + 8 * PB_COUNT + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int part = static_cast<int>(blockIdx.x) / p.tiles_per_part;
+    const int ntile = static_cast<int>(blockIdx.x) - part * p.tiles_per_part;
+    const int m0 = static_cast<int>(blockIdx.y) * T::BM;
+    const int nk = p.n_kblocks;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < T::STAGES; ++s) {
+            mbar_init(bar(PB_FULL + s), 1);
+            mbar_init(bar(PB_EMPTY + s), 1);
+        }
+        mbar_init(bar(PB_ACC), 1);
+        mbar_init(bar(PB_DRAIN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc<256>(smem_u32(tmem_slot));
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl ctl{abort_flag, p.wait_limit_ns, p.status, 3u};
+    const uint32_t sA = sbase + T::OFF_A, sB = sbase + T::OFF_B;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const int wrow = part * p.inner + p.wrow0 + ntile * T::BN;
+            int last = -1;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % T::STAGES, u = kb / T::STAGES;
+                if (u > 0 && !mbar_wait(bar(PB_EMPTY + s), (u - 1) & 1, ctl, 1)) break;
+                mbar_arrive_expect_tx(bar(PB_FULL + s), T::A_BYTES + T::B_BYTES);
+                tma_load_2d(sA + s * T::A_BYTES, &tmX, bar(PB_FULL + s), kb * T::BK, m0);
+                tma_load_2d(sB + s * T::B_BYTES, &tmW, bar(PB_FULL + s), kb * T::BK, wrow);
+                last = kb;
+            }
+            if (*abort_flag) {
+                for (int kb = last; kb >= 0 && kb > last - T::STAGES; --kb)
+                    proj_drain_wait(bar(PB_FULL + kb % T::STAGES), (kb / T::STAGES) & 1, p.wait_limit_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint64_t dA = smem_desc_sw128(sA, 16, 1024);
+            const uint64_t dB = smem_desc_sw128(sB, 16, 1024);
+            constexpr uint64_t kStageA = T::A_BYTES >> 4, kStageB = T::B_BYTES >> 4;
+            bool ok = true;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % T::STAGES, u = kb / T::STAGES;
+                if (!mbar_wait(bar(PB_FULL + s), u & 1, ctl, 10)) { ok = false; break; }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < T::BK / 32; ++kk)  // K = 32 bytes per MMA
+                    mma_f8(tmem, dA + s * kStageA + kk * 2, dB + s * kStageB + kk * 2, T::IDESC,
+                           (kb > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(PB_EMPTY + s));
+            }
+            if (ok) {
+                mma_commit(bar(PB_ACC));
+            } else {
+                mma_commit(bar(PB_DRAIN));
+                proj_drain_wait(bar(PB_DRAIN), 0, p.wait_limit_ns);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int wq = warp & 3;  // TMEM lane quarter of this warp
+        const int row = m0 + wq * 32 + lane;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        if (__all_sync(0xffffffffu, mbar_wait(bar(PB_ACC), 0, ctl, 20))) {
+            tc_fence_after_sync();
+            __nv_bfloat16* dst = p.out[part] + static_cast<size_t>(row) * p.Nr + ntile * T::BN;
+            const int cols = min(T::BN, p.Nr - ntile * T::BN);  // multiple of 8
+#pragma unroll 1
+            for (int c = 0; c < T::BN / 32; ++c) {
+                float a[32];
+                tmem_ld32(lane_addr + 32 * c, a);
+                if (row < p.S && 32 * c < cols) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+                    const int nv = min(4, (cols - 32 * c) / 8);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        if (v < nv) {
+                            uint4 wv;
+                            wv.x = pack_bf16x2(a[8 * v + 0] * p.scale, a[8 * v + 1] * p.scale);
+                            wv.y = pack_bf16x2(a[8 * v + 2] * p.scale, a[8 * v + 3] * p.scale);
+                            wv.z = pack_bf16x2(a[8 * v + 4] * p.scale, a[8 * v + 5] * p.scale);
+                            wv.w = pack_bf16x2(a[8 * v + 6] * p.scale, a[8 * v + 7] * p.scale);
+                            d4[v] = wv;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<256>(tmem);
+    }
+}
+
+int launch_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, void* k_out, void* v_out, int S,
+                        int hidden, int inner, int P, int rank, cudaStream_t stream) {
+    using T = ProjTraits;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e =
+            cudaFuncSetAttribute(qkv_proj_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e);
+        attr_done = true;
+    }
+    CUtensorMap mx, mw;
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(hidden), static_cast<cuuint64_t>(S)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(hidden)};
+        const cuuint32_t box[2] = {T::BK, T::BM};
+        const cuuint32_t estr[2] = {1, 1};
+        int rc = encode_tensor_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, x, dims, strides, box, estr,
+                                   CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != H3ATTN_OK) return rc;
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(hidden), static_cast<cuuint64_t>(3) * inner};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(hidden)};
+        const cuuint32_t box[2] = {T::BK, T::BN};
+        const cuuint32_t estr[2] = {1, 1};
+        int rc = encode_tensor_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, w, dims, strides, box, estr,
+                                   CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != H3ATTN_OK) return rc;
+    }
+    ProjParams prm;
+    prm.out[0] = static_cast<__nv_bfloat16*>(q_out);
+    prm.out[1] = static_cast<__nv_bfloat16*>(k_out);
+    prm.out[2] = static_cast<__nv_bfloat16*>(v_out);
+    prm.S = S;
+    prm.Nr = inner / P;
+    prm.wrow0 = rank * (inner / P);
+    prm.inner = inner;
+    prm.n_kblocks = (hidden + T::BK - 1) / T::BK;
+    prm.tiles_per_part = (prm.Nr + T::BN - 1) / T::BN;
+    prm.scale = scale;
+    prm.wait_limit_ns = wait_limit_ns();
+    int rc = device_status_ptr(&prm.status);
+    if (rc != H3ATTN_OK) return rc;
+    const dim3 grid(static_cast<unsigned>(3 * prm.tiles_per_part), static_cast<unsigned>((S + T::BM - 1) / T::BM));
+    qkv_proj_fp8_kernel<<<grid, kProjThreads, T::SMEM_BYTES, stream>>>(mx, mw, prm);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e);
+}
+
+}  // namespace h3

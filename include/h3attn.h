@@ -156,6 +156,26 @@ H3ATTN_API int h3attn_head2seq_heads(const void* in_group, void* out, int S, int
                                      int head_begin, int head_count, void* stream);
 
 /*
+ * h3attn_qkv_proj_fp8 -- the all-gather exchange variant's projection: the
+ * gathered hidden state times only this rank's head rows of qkv_proj
+ * ("buqi-minimax-h3-multigpu" README, "How it works": for world sizes up to
+ * 4 each rank receives the modulated hidden state and projects it through its
+ * own head rows of qkv_proj; slicing the fp8 weight by rows is exact because
+ * its scale is one number per tensor).  For part in (q, k, v):
+ *     out_part[s][c] = scale * sum_e x[s][e] * w[part*inner + rank*inner/P + c][e]
+ *   x       [S][hidden] FP8 E4M3 codes (hidden % 16 == 0).
+ *   w       [3*inner][hidden] FP8 E4M3 codes: q rows, then k rows, then v
+ *           rows; head h of a part owns rows [h*D, (h+1)*D) of it.
+ *   scale   product of the two per-tensor scales (applied in fp32).
+ *   q_out, k_out, v_out  [S][inner/P] bf16 each, i.e. [S][H/P][D]: this
+ *           rank's heads in the layout h3attn_forward reads.  (inner/P) % 8 == 0.
+ *   0 <= rank < P.  FP8 products, fp32 accumulation; the result for a given
+ *   (s, part, global column) is bit-identical for every P and rank.
+ */
+H3ATTN_API int h3attn_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, void* k_out,
+                                   void* v_out, int S, int hidden, int inner, int P, int rank, void* stream);
+
+/*
  * h3attn_get_device_status -- synchronise `stream`, then read and clear the
  * device status word of the current device.  Returns H3ATTN_OK,
  * H3ATTN_ERR_DEVICE_TIMEOUT (a kernel gave up on a wait, wrote nothing
