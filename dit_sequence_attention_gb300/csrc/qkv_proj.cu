@@ -9,15 +9,18 @@
 // for part in (q, k, v) and c < inner/P, written as bf16 [S][inner/P] per part
 // (the head-sharded [S][H/P][D] layout the attention kernel reads).
 //
-// One CTA = 128 tokens x 256 output features of one part, 192 threads:
-//   warp 0      TMA producer: x and w tiles of 128 bytes along K into a
-//               4-stage ring (128B swizzle).
-//   warp 1      allocates 256 TMEM columns; one lane issues 4 MMAs (K = 32)
-//               per stage with descriptors built once (start address offsets).
-//   warps 2-5   epilogue: TMEM -> registers, times scale, bf16, global stores.
-// The grid walks the output-feature tiles fastest, so the CTAs that run at the
-// same time share their x rows through L2; the weight slice (58 MB at P = 2)
-// stays L2-resident.  Each output element's K accumulation order is the same
+// Persistent: one CTA per SM walks output tiles of 128 tokens x 256 output
+// features of one part (tile t, t + grid, ...), 192 threads:
+//   warp 0      TMA producer: x and w slices of 128 bytes along K into a
+//               4-stage ring (128B swizzle) that runs across tiles.
+//   warp 1      allocates 512 TMEM columns = two 128x256 fp32 accumulators;
+//               one lane issues 4 MMAs (K = 32) per stage with descriptors
+//               built once (start-address offsets only).
+//   warps 2-5   epilogue: TMEM -> registers, times scale, bf16, global stores;
+//               while they drain one accumulator the MMAs fill the other.
+// Tiles are numbered with the output-feature tile fastest, so the CTAs that
+// run at the same time share their x rows through L2; the weight slice
+// (58 MB at P = 2) stays L2-resident.  Each output element's K accumulation order is the same
 // whatever the rank or tile, so the per-rank projections are bit-identical to
 // the matching columns of the full (P = 1) projection.
 #include <cuda.h>
@@ -40,13 +43,14 @@ struct ProjTraits {
     static constexpr int OFF_B = STAGES * A_BYTES;
     static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
     static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+    static constexpr int ACC_COLS = BN;  // fp32 accumulator columns per tile
     // kind::f8f6f4: D = f32 (bit 4), A = B = E4M3 (format 0), K-major, N >> 3, M >> 4
     static constexpr uint32_t IDESC =
         (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
     static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 };
 
-enum : int { PB_FULL = 0, PB_EMPTY = 4, PB_ACC = 8, PB_DRAIN = 9, PB_COUNT = 10 };
+enum : int { PB_FULL = 0, PB_EMPTY = 4, PB_ACC = 8, PB_ACCFREE = 10, PB_DRAIN = 12, PB_COUNT = 13 };
 
 struct ProjParams {
     __nv_bfloat16* out[3];  // q, k, v: [S][Nr] bf16
@@ -56,6 +60,8 @@ struct ProjParams {
     int inner;
     int n_kblocks;
     int tiles_per_part;
+    int n_tiles_n;          // 3 * tiles_per_part
+    int n_tiles;            // n_tiles_n * token tiles
     float scale;
     unsigned long long wait_limit_ns;
     DeviceStatus* status;
@@ -100,9 +106,6 @@ __global__ void __launch_bounds__(kProjThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int part = static_cast<int>(blockIdx.x) / p.tiles_per_part;
-    const int ntile = static_cast<int>(blockIdx.x) - part * p.tiles_per_part;
-    const int m0 = static_cast<int>(blockIdx.y) * T::BM;
     const int nk = p.n_kblocks;
 
     if (threadIdx.x == 0) {
@@ -110,13 +113,16 @@ __global__ void __launch_bounds__(kProjThreads, 1)
             mbar_init(bar(PB_FULL + s), 1);
             mbar_init(bar(PB_EMPTY + s), 1);
         }
-        mbar_init(bar(PB_ACC), 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar(PB_ACC + a), 1);
+            mbar_init(bar(PB_ACCFREE + a), 4);  // one elected lane per epilogue warp
+        }
         mbar_init(bar(PB_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc<256>(smem_u32(tmem_slot));
+        tmem_alloc<512>(smem_u32(tmem_slot));
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
@@ -133,19 +139,25 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const int wrow = part * p.inner + p.wrow0 + ntile * T::BN;
+            int it = 0;   // position in the smem ring, continuous across tiles
             int last = -1;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % T::STAGES, u = kb / T::STAGES;
-                if (u > 0 && !mbar_wait(bar(PB_EMPTY + s), (u - 1) & 1, ctl, 1)) break;
-                mbar_arrive_expect_tx(bar(PB_FULL + s), T::A_BYTES + T::B_BYTES);
-                tma_load_2d(sA + s * T::A_BYTES, &tmX, bar(PB_FULL + s), kb * T::BK, m0);
-                tma_load_2d(sB + s * T::B_BYTES, &tmW, bar(PB_FULL + s), kb * T::BK, wrow);
-                last = kb;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x) {
+                const int nt = tile % p.n_tiles_n, mt = tile / p.n_tiles_n;
+                const int part = nt / p.tiles_per_part, ntile = nt - part * p.tiles_per_part;
+                const int wrow = part * p.inner + p.wrow0 + ntile * T::BN;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % T::STAGES, u = it / T::STAGES;
+                    if (u > 0 && !mbar_wait(bar(PB_EMPTY + s), (u - 1) & 1, ctl, 1)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bar(PB_FULL + s), T::A_BYTES + T::B_BYTES);
+                    tma_load_2d(sA + s * T::A_BYTES, &tmX, bar(PB_FULL + s), kb * T::BK, mt * T::BM);
+                    tma_load_2d(sB + s * T::B_BYTES, &tmW, bar(PB_FULL + s), kb * T::BK, wrow);
+                    last = it;
+                }
             }
             if (*abort_flag) {
-                for (int kb = last; kb >= 0 && kb > last - T::STAGES; --kb)
-                    proj_drain_wait(bar(PB_FULL + kb % T::STAGES), (kb / T::STAGES) & 1, p.wait_limit_ns);
+                for (int i = last; i >= 0 && i > last - T::STAGES; --i)
+                    proj_drain_wait(bar(PB_FULL + i % T::STAGES), (i / T::STAGES) & 1, p.wait_limit_ns);
             }
         }
     } else if (warp == 1) {
@@ -155,19 +167,25 @@ __global__ void __launch_bounds__(kProjThreads, 1)
             const uint64_t dB = smem_desc_sw128(sB, 16, 1024);
             constexpr uint64_t kStageA = T::A_BYTES >> 4, kStageB = T::B_BYTES >> 4;
             bool ok = true;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % T::STAGES, u = kb / T::STAGES;
-                if (!mbar_wait(bar(PB_FULL + s), u & 1, ctl, 10)) { ok = false; break; }
+            int it = 0, n_local = 0;
+            for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++n_local) {
+                const int acc = n_local & 1, use = n_local >> 1;
+                if (use > 0 && !mbar_wait(bar(PB_ACCFREE + acc), (use - 1) & 1, ctl, 11)) { ok = false; break; }
                 tc_fence_after_sync();
+                const uint32_t d = tmem + acc * T::ACC_COLS;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % T::STAGES, u = it / T::STAGES;
+                    if (!mbar_wait(bar(PB_FULL + s), u & 1, ctl, 10)) { ok = false; break; }
+                    tc_fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < T::BK / 32; ++kk)  // K = 32 bytes per MMA
-                    mma_f8(tmem, dA + s * kStageA + kk * 2, dB + s * kStageB + kk * 2, T::IDESC,
-                           (kb > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(PB_EMPTY + s));
+                    for (int kk = 0; kk < T::BK / 32; ++kk)  // K = 32 bytes per MMA
+                        mma_f8(d, dA + s * kStageA + kk * 2, dB + s * kStageB + kk * 2, T::IDESC,
+                               (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(PB_EMPTY + s));
+                }
+                if (ok) mma_commit(bar(PB_ACC + acc));
             }
-            if (ok) {
-                mma_commit(bar(PB_ACC));
-            } else {
+            if (!ok) {
                 mma_commit(bar(PB_DRAIN));
                 proj_drain_wait(bar(PB_DRAIN), 0, p.wait_limit_ns);
             }
@@ -175,16 +193,22 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int wq = warp & 3;  // TMEM lane quarter of this warp
-        const int row = m0 + wq * 32 + lane;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        if (__all_sync(0xffffffffu, mbar_wait(bar(PB_ACC), 0, ctl, 20))) {
+        int n_local = 0;
+        for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++n_local) {
+            const int acc = n_local & 1, use = n_local >> 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(PB_ACC + acc), use & 1, ctl, 20))) break;
             tc_fence_after_sync();
-            __nv_bfloat16* dst = p.out[part] + static_cast<size_t>(row) * p.Nr + ntile * T::BN;
+            const int nt = tile % p.n_tiles_n, mt = tile / p.n_tiles_n;
+            const int part = nt / p.tiles_per_part, ntile = nt - part * p.tiles_per_part;
+            const int row = mt * T::BM + wq * 32 + lane;
+            __nv_bfloat16* base = part == 0 ? p.out[0] : (part == 1 ? p.out[1] : p.out[2]);
+            __nv_bfloat16* dst = base + static_cast<size_t>(row) * p.Nr + ntile * T::BN;
             const int cols = min(T::BN, p.Nr - ntile * T::BN);  // multiple of 8
 #pragma unroll 1
             for (int c = 0; c < T::BN / 32; ++c) {
                 float a[32];
-                tmem_ld32(lane_addr + 32 * c, a);
+                tmem_ld32(lane_addr + acc * T::ACC_COLS + 32 * c, a);
                 if (row < p.S && 32 * c < cols) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
                     const int nv = min(4, (cols - 32 * c) / 8);
@@ -201,6 +225,9 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                     }
                 }
             }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(PB_ACCFREE + acc));
         }
     }
 
@@ -208,7 +235,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc<256>(tmem);
+        tmem_dealloc<512>(tmem);
     }
 }
 
@@ -251,11 +278,20 @@ int launch_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, 
     prm.inner = inner;
     prm.n_kblocks = (hidden + T::BK - 1) / T::BK;
     prm.tiles_per_part = (prm.Nr + T::BN - 1) / T::BN;
+    prm.n_tiles_n = 3 * prm.tiles_per_part;
+    prm.n_tiles = prm.n_tiles_n * ((S + T::BM - 1) / T::BM);
     prm.scale = scale;
     prm.wait_limit_ns = wait_limit_ns();
     int rc = device_status_ptr(&prm.status);
     if (rc != H3ATTN_OK) return rc;
-    const dim3 grid(static_cast<unsigned>(3 * prm.tiles_per_part), static_cast<unsigned>((S + T::BM - 1) / T::BM));
+    static int n_sm = 0;
+    if (n_sm == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    const unsigned grid = static_cast<unsigned>(min(prm.n_tiles, n_sm));
     qkv_proj_fp8_kernel<<<grid, kProjThreads, T::SMEM_BYTES, stream>>>(mx, mw, prm);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e);
