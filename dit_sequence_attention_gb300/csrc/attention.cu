@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(B_SFULL + t), 1);
-            mbar_init(bar(B_PFULL + t), 128);
+            mbar_init(bar(B_PFULL + t), 4);   // one elected lane per softmax warp
             mbar_init(bar(B_OFINAL + t), 1);
         }
         mbar_init(bar(B_DRAIN), 1);
@@ -361,7 +361,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before_sync();
-            mbar_arrive(bar(B_PFULL + wg));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_PFULL + wg));
         }
         // ---------------------------------------------------------- epilogue
         if (ok && __all_sync(0xffffffffu, mbar_wait(bar(B_OFINAL + wg), 0, ctl, 24 + wg))) {
