@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstdint>
 #include <cstdlib>
 #include <cmath>
@@ -136,6 +138,13 @@ static int check_layout_args(const void* in, const void* out, int S, int H, int 
     return H3ATTN_OK;
 }
 
+// NVTX range around each entry point (header-only NVTX v3: a no-op unless a
+// profiler is attached), so timelines show which library call issued a kernel.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
+
 }  // namespace h3
 
 using namespace h3;
@@ -164,6 +173,7 @@ const char* h3attn_strerror(int code) {
 int h3attn_qk_norm_rope(const void* q, const void* k, void* q_out, void* k_out, float* dbg_fp32,
                         const float* w_q, const float* w_k, const int32_t* pos, int B, int S, int H, int D,
                         int d_t, int d_h, int d_w, float eps, float theta, void* stream) {
+    const NvtxRange nvtx_range("h3attn_qk_norm_rope");
     if (!q || !k || !q_out || !k_out || !w_q || !w_k || !pos) return H3ATTN_ERR_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(w_q) ||
         !aligned16(w_k) || (dbg_fp32 && !aligned16(dbg_fp32)))
@@ -188,6 +198,7 @@ int h3attn_qk_norm_rope(const void* q, const void* k, void* q_out, void* k_out, 
 int h3attn_qk_norm_rope_seq2head(const void* q, const void* k, void* qh_out, void* kh_out, float* dbg_fp32,
                                  const float* w_q, const float* w_k, const int32_t* pos, int S, int H, int D,
                                  int P, int d_t, int d_h, int d_w, float eps, float theta, void* stream) {
+    const NvtxRange nvtx_range("h3attn_qk_norm_rope_seq2head");
     if (!q || !k || !qh_out || !kh_out || !w_q || !w_k || !pos) return H3ATTN_ERR_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(qh_out) || !aligned16(kh_out) || !aligned16(w_q) ||
         !aligned16(w_k) || (dbg_fp32 && !aligned16(dbg_fp32)))
@@ -211,6 +222,7 @@ int h3attn_qk_norm_rope_seq2head(const void* q, const void* k, void* qh_out, voi
 
 int h3attn_forward(const void* q, const void* k, const void* v, void* o, int B, int S, int H_buf, int D,
                    int head_begin, int head_count, const int32_t* kv_len, float scale, void* stream) {
+    const NvtxRange nvtx_range("h3attn_forward");
     if (!q || !k || !v || !o) return H3ATTN_ERR_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return H3ATTN_ERR_ARG;
     if (!(scale == scale)) return H3ATTN_ERR_ARG;  // NaN
@@ -239,6 +251,7 @@ int h3attn_forward(const void* q, const void* k, const void* v, void* o, int B, 
 }
 
 int h3attn_seq2head(const void* in, void* out, int S, int H, int D, int P, void* stream) {
+    const NvtxRange nvtx_range("h3attn_seq2head");
     int rc = check_layout_args(in, out, S, H, D, P);
     if (rc != H3ATTN_OK) return rc;
     if ((rc = check_device()) != H3ATTN_OK) return rc;
@@ -246,6 +259,7 @@ int h3attn_seq2head(const void* in, void* out, int S, int H, int D, int P, void*
 }
 
 int h3attn_head2seq(const void* in, void* out, int S, int H, int D, int P, void* stream) {
+    const NvtxRange nvtx_range("h3attn_head2seq");
     int rc = check_layout_args(in, out, S, H, D, P);
     if (rc != H3ATTN_OK) return rc;
     if ((rc = check_device()) != H3ATTN_OK) return rc;
@@ -254,6 +268,7 @@ int h3attn_head2seq(const void* in, void* out, int S, int H, int D, int P, void*
 
 int h3attn_head2seq_heads(const void* in_group, void* out, int S, int H, int D, int P, int group,
                           int head_begin, int head_count, void* stream) {
+    const NvtxRange nvtx_range("h3attn_head2seq_heads");
     if (in_group == nullptr || out == nullptr) return H3ATTN_ERR_ARG;
     if (!aligned16(in_group) || !aligned16(out)) return H3ATTN_ERR_ARG;
     if (S < 1 || H < 1 || P < 1 || (D != 64 && D != 128) || H % P != 0) return H3ATTN_ERR_SHAPE;
@@ -272,6 +287,7 @@ int h3attn_head2seq_heads(const void* in_group, void* out, int S, int H, int D, 
 
 int h3attn_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, void* k_out, void* v_out, int S,
                         int hidden, int inner, int P, int rank, void* stream) {
+    const NvtxRange nvtx_range("h3attn_qkv_proj_fp8");
     if (!x || !w || !q_out || !k_out || !v_out) return H3ATTN_ERR_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(v_out))
         return H3ATTN_ERR_ARG;
