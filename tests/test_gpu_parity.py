@@ -303,3 +303,42 @@ def test_head2seq_heads_writes_only_its_heads(h3, cuda_device):
     mask = torch.ones(H, dtype=torch.bool)
     mask[sel] = False
     assert torch.isnan(out[:, mask].float()).all()
+
+
+# ------------------------------------------------------- batch and scale
+def test_attention_batch_with_per_item_kv_len_and_explicit_scale(h3, cuda_device):
+    B, S, H, D = 3, 384, 2, 128
+    kvs = [384, 130, 1]
+    q, k, v = (synth.randn_bf16((B, S, H, D), 100 + i, cuda_device) for i in range(3))
+    o = torch.empty_like(q)
+    scale = 0.05
+    h3.h3attn_forward(q, k, v, o, kv_len=kvs, scale=scale)
+    assert h3.h3attn_get_device_status() == 0
+    for b in range(B):
+        ref = oracle.attention(oracle.bf16_to_f64(q[b]), oracle.bf16_to_f64(k[b]), oracle.bf16_to_f64(v[b]),
+                               kv_len=kvs[b], scale=scale)
+        err = per_head_rel_err(o[b].float().cpu().numpy(), ref)
+        assert np.all(err <= ATTN_TOL), f"batch item {b}: {err}"
+        # each item equals a single-item call on its own slice
+        o1 = torch.empty_like(q[b])
+        h3.h3attn_forward(q[b], k[b], v[b], o1, kv_len=kvs[b], scale=scale)
+        assert torch.equal(o1.view(torch.int16), o[b].view(torch.int16))
+
+
+def test_norm_rope_batch_shares_positions(h3, cuda_device):
+    B, S, H, D = 2, 96, 4, 64
+    w = synth.WORKLOADS["tiny"]
+    q, k = synth.randn_bf16((B, S, H, D), 110, cuda_device), synth.randn_bf16((B, S, H, D), 111, cuda_device)
+    wq, wk = (t.to(cuda_device) for t in synth.norm_weights(D))
+    pos_np = synth.packed_positions(w)[:S]
+    pos = torch.from_numpy(pos_np).to(cuda_device)
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    dbg = torch.empty((2, B, S, H, D), dtype=torch.float32, device=cuda_device)
+    h3.h3attn_qk_norm_rope(q, k, qo, ko, wq, wk, pos, *w.rope_split, w.eps, w.theta, dbg_fp32=dbg)
+    assert h3.h3attn_get_device_status() == 0
+    for b in range(B):
+        for i, (src, wt) in enumerate(((q, wq), (k, wk))):
+            ref = oracle.norm_rope(oracle.bf16_to_f64(src[b]), wt.double().cpu().numpy(), pos_np, w.eps,
+                                   *w.rope_split, w.theta)
+            got = dbg[i, b].cpu().numpy()
+            assert np.abs(got - ref).max() / np.abs(ref).max() <= NORM_TOL
