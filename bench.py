@@ -468,7 +468,10 @@ def main():
     cpu = None
     if not args.no_cpu_baseline:
         f, dt, desc, threads = cpu_oracle_sample(w, args.cpu_seconds)
-        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "sample_seconds": dt,
+               "extrapolated_full_step_s": w.attention_flops() / (f / dt),
+               "note": "extrapolated: the whole 56-head step at the sample's measured rate"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

@@ -416,15 +416,9 @@ template <int D>
 static int launch_one(const void* q, const void* k, const void* v, void* o, int S, int H_buf, int head_begin,
                       int head_count, int kv_len, float scale, cudaStream_t stream) {
     using T = AttnTraits<D>;
-    static bool attr_done = false;  // per process; set on first successful use
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             T::SMEM_BYTES);
-        if (e != cudaSuccess) return cuda_fail(e);
-        attr_done = true;
-    }
+    int rc = ensure_smem_attr(reinterpret_cast<const void*>(attn_fwd_kernel<D>), T::SMEM_BYTES);
+    if (rc != H3ATTN_OK) return rc;
     CUtensorMap mq, mk, mv;
-    int rc;
     if ((rc = encode_rows_map(&mq, q, D, H_buf, S)) != H3ATTN_OK) return rc;
     if ((rc = encode_rows_map(&mk, k, D, H_buf, kv_len)) != H3ATTN_OK) return rc;
     if ((rc = encode_rows_map(&mv, v, D, H_buf, kv_len)) != H3ATTN_OK) return rc;

@@ -17,6 +17,10 @@ int device_status_ptr(DeviceStatus** out);
 // Records `e` as this thread's last CUDA error and returns H3ATTN_ERR_CUDA.
 int cuda_fail(cudaError_t e);
 
+// Sets the kernel's dynamic shared-memory limit once per device (the
+// attribute is per device; a process may drive several GPUs).
+int ensure_smem_attr(const void* kernel, int bytes);
+
 // Per-wait time limit handed to the kernels (nanoseconds).  2 s unless the
 // environment variable H3ATTN_WAIT_LIMIT_NS overrides it.
 unsigned long long wait_limit_ns();

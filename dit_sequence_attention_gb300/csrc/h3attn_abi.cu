@@ -37,6 +37,29 @@ int device_status_ptr(DeviceStatus** out) {
     return H3ATTN_OK;
 }
 
+int ensure_smem_attr(const void* kernel, int bytes) {
+    constexpr int kMaxDevices = 64;
+    constexpr int kMaxKernels = 8;
+    static const void* done[kMaxDevices][kMaxKernels] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return H3ATTN_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < kMaxKernels; ++i) {
+        if (done[dev][i] == kernel) return H3ATTN_OK;
+        if (done[dev][i] == nullptr) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            if (e != cudaSuccess) return cuda_fail(e);
+            done[dev][i] = kernel;
+            return H3ATTN_OK;
+        }
+    }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e);
+}
+
 static thread_local int t_last_cuda_error = 0;
 static unsigned long long g_last_info = 0;
 

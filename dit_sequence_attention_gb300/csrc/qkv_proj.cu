@@ -283,12 +283,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
 int launch_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, void* k_out, void* v_out, int S,
                         int hidden, int inner, int P, int rank, cudaStream_t stream) {
     using T = ProjTraits;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e =
-            cudaFuncSetAttribute(qkv_proj_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
-        if (e != cudaSuccess) return cuda_fail(e);
-        attr_done = true;
+    {
+        const int rc = ensure_smem_attr(reinterpret_cast<const void*>(qkv_proj_fp8_kernel), T::SMEM_BYTES);
+        if (rc != H3ATTN_OK) return rc;
     }
     CUtensorMap mx, mw;
     {
@@ -325,8 +322,8 @@ int launch_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, 
     prm.wait_limit_ns = wait_limit_ns();
     int rc = device_status_ptr(&prm.status);
     if (rc != H3ATTN_OK) return rc;
-    static int n_sm = 0;
-    if (n_sm == 0) {
+    int n_sm = 0;
+    {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
