@@ -235,20 +235,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mma_commit(bar(B_SFULL + 1));
                 mma_commit(bar(B_KEMPTY + 0));
             }
+            // The TMA barriers of the next step are waited right after the last
+            // MMA group of this one, where the thread would soon wait for P
+            // anyway: a waiting thread lets its queued MMAs drain, so between
+            // PV_0 and QK_0 (and PV_1, QK_1) the stream is never broken.
+            ok = ok && mbar_wait(bar(B_VFULL + 0), 0, ctl, 12) && (n < 2 || mbar_wait(bar(B_KFULL + 1 % T::KST), 0, ctl, 14));
             for (int j = 0; j < n && ok; ++j) {
-                const int vs = j % T::VST, vu = j / T::VST;
+                const int vs = j % T::VST;
                 const bool more = (j + 1) < n;
-                const int ks = (j + 1) % T::KST, ku = (j + 1) / T::KST;
+                const int ks = (j + 1) % T::KST;
                 const uint64_t dVj = dV + vs * kStage;
-                if (!mbar_wait(bar(B_VFULL + vs), vu & 1, ctl, 12) || !mbar_wait(bar(B_PFULL + 0), j & 1, ctl, 13)) {
-                    ok = false;
-                    break;
-                }
+                if (!mbar_wait(bar(B_PFULL + 0), j & 1, ctl, 13)) { ok = false; break; }
                 tc_fence_after_sync();
                 issue_pv<D>(tmem + T::COL_O0, tmem + T::COL_S0, dVj, j > 0);
                 if (more) {
-                    if (!mbar_wait(bar(B_KFULL + ks), ku & 1, ctl, 14)) { ok = false; break; }
-                    tc_fence_after_sync();
                     issue_qk<D>(tmem + T::COL_S0, dQ0, dK + ks * kStage);
                     mma_commit(bar(B_SFULL + 0));
                 } else {
@@ -262,6 +262,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     issue_qk<D>(tmem + T::COL_S1, dQ1, dK + ks * kStage);
                     mma_commit(bar(B_SFULL + 1));
                     mma_commit(bar(B_KEMPTY + ks));
+                    // next step's V tile and the key tile after next
+                    const int jv = j + 1, jk = j + 2;
+                    if (!mbar_wait(bar(B_VFULL + jv % T::VST), (jv / T::VST) & 1, ctl, 12) ||
+                        (jk < n && !mbar_wait(bar(B_KFULL + jk % T::KST), (jk / T::KST) & 1, ctl, 14))) {
+                        ok = false;
+                        break;
+                    }
                 } else {
                     mma_commit(bar(B_OFINAL + 1));
                 }
