@@ -5,6 +5,12 @@ The functions here only check and marshal torch tensors into the C calls of
 the same names; every step of the path runs in the library's CUDA kernels.
 There is no fallback: if the library is missing or the device is not an
 sm_103 GPU, calls raise.
+
+Two builds of the same kernels exist: ``libh3attn.so`` and
+``libh3attn_debug.so``, in which every kernel checks its computed indices and
+reports a failed check as H3ATTN_ERR_DEVICE_BOUNDS instead of touching memory
+outside its buffers.  The debug build is used when the environment variable
+``H3ATTN_DEBUG`` is ``1`` at the first call, or after ``use_debug_checks(True)``.
 """
 from __future__ import annotations
 
@@ -18,13 +24,14 @@ __all__ = [
     "h3attn_qk_norm_rope", "h3attn_qk_norm_rope_seq2head", "h3attn_forward", "h3attn_seq2head",
     "h3attn_head2seq", "h3attn_head2seq_heads", "h3attn_qkv_proj_fp8",
     "h3attn_get_device_status", "h3attn_strerror", "h3attn_version", "h3attn_selftest_wait_timeout",
-    "h3attn_last_device_error_info",
+    "h3attn_last_device_error_info", "h3attn_build_flags", "h3attn_selftest_bounds", "use_debug_checks",
     "ulysses_attention_step",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_PKG, "libh3attn.so")
-_lib = None
+_LIB_PATHS = {False: os.path.join(_PKG, "libh3attn.so"), True: os.path.join(_PKG, "libh3attn_debug.so")}
+_libs = {}
+_debug = os.environ.get("H3ATTN_DEBUG", "") == "1"
 
 H3ATTN_OK = 0
 H3ATTN_ERR_ARG = -1
@@ -33,6 +40,8 @@ H3ATTN_ERR_ALIAS = -3
 H3ATTN_ERR_CUDA = -4
 H3ATTN_ERR_DEVICE_TIMEOUT = -5
 H3ATTN_ERR_UNSUPPORTED_DEVICE = -6
+H3ATTN_ERR_DEVICE_BOUNDS = -7
+H3ATTN_BUILD_DEBUG_CHECKS = 1
 
 # exported symbol -> (restype, argtypes)
 _P, _I, _F, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
@@ -50,6 +59,8 @@ SIGNATURES = {
     "h3attn_strerror": (ctypes.c_char_p, [_I]),
     "h3attn_version": (_I, []),
     "h3attn_selftest_wait_timeout": (_I, [_U64, _P]),
+    "h3attn_build_flags": (_I, []),
+    "h3attn_selftest_bounds": (_I, [_P, _U64, _P]),
 }
 
 
@@ -63,23 +74,32 @@ class H3AttnError(RuntimeError):
 
 
 def library_path() -> str:
-    return _LIB_PATH
+    return _LIB_PATHS[_debug]
+
+
+def use_debug_checks(enable: bool) -> None:
+    """Route every following call to libh3attn_debug.so (True) or libh3attn.so
+    (False).  Each library keeps its own device status word."""
+    global _debug
+    _debug = bool(enable)
 
 
 def load_library():
-    """Load libh3attn.so (built in-tree by ``dit_sequence_attention_gb300.build``)."""
-    global _lib
-    if _lib is None:
-        if not os.path.exists(_LIB_PATH):
-            raise RuntimeError(f"{_LIB_PATH} is not built; run `python -m dit_sequence_attention_gb300.build` "
+    """Load the selected build (built in-tree by ``dit_sequence_attention_gb300.build``)."""
+    lib = _libs.get(_debug)
+    if lib is None:
+        path = _LIB_PATHS[_debug]
+        if not os.path.exists(path):
+            flag = " --debug" if _debug else ""
+            raise RuntimeError(f"{path} is not built; run `python -m dit_sequence_attention_gb300.build{flag}` "
                                "(or __graft_entry__.build()) first")
-        lib = ctypes.CDLL(_LIB_PATH)
+        lib = ctypes.CDLL(path)
         for name, (res, args) in SIGNATURES.items():
             f = getattr(lib, name)
             f.restype = res
             f.argtypes = args
-        _lib = lib
-    return _lib
+        _libs[_debug] = lib
+    return lib
 
 
 def _stream_ptr(stream) -> int:
@@ -276,6 +296,20 @@ def h3attn_last_device_error_info() -> int:
 def h3attn_selftest_wait_timeout(limit_ns: int, stream=None):
     rc = load_library().h3attn_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream))
     _check("h3attn_selftest_wait_timeout", rc)
+
+
+def h3attn_build_flags() -> int:
+    return int(load_library().h3attn_build_flags())
+
+
+def h3attn_selftest_bounds(buf: torch.Tensor, stream=None):
+    """Self-test of the device index checks (debug build only): ``buf`` is a
+    CUDA tensor of at least 1024 bytes, overwritten.  Read the outcome with
+    ``h3attn_get_device_status()`` (H3ATTN_ERR_DEVICE_BOUNDS expected)."""
+    if not isinstance(buf, torch.Tensor) or not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    rc = load_library().h3attn_selftest_bounds(buf.data_ptr(), buf.numel() * buf.element_size(), _stream_ptr(stream))
+    _check("h3attn_selftest_bounds", rc)
 
 
 def ulysses_attention_step(q, k, v, w_q, w_k, pos, P, kv_len, d_t, d_h, d_w, eps=1e-6, theta=10000.0,

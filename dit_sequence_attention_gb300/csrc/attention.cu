@@ -89,6 +89,7 @@ struct AttnParams {
     float scale_log2;   // softmax scale * log2(e)
     unsigned long long wait_limit_ns;
     DeviceStatus* status;
+    unsigned long long o_elems;  // S * H_buf * D: extent of `o` (index checks of debug-check builds)
 };
 
 // Wait for an mbarrier phase ignoring the abort flag (used only on the abort
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const WaitCtl ctl{abort_flag, p.wait_limit_ns, p.status, 1u};
+    const WaitCtl ctl{abort_flag, p.wait_limit_ns, p.status, kTagAttention};
 
     const uint32_t sQ = sbase + T::OFF_Q, sK = sbase + T::OFF_K, sV = sbase + T::OFF_V;
 
@@ -381,7 +382,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int c = 0; c < D / 32; ++c) {
                 float o32[32];
                 tmem_ld32(lane_addr + colO + 32 * c, o32);
-                if (row < p.S) {
+                if (row < p.S && in_bounds(p.status, (static_cast<size_t>(row) * p.H_buf + head) * D + 32 * c, 32,
+                                           p.o_elems, kTagAttention, 1)) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -438,6 +440,7 @@ static int launch_one(const void* q, const void* k, const void* v, void* o, int 
     prm.n_kv_tiles = (kv_len + T::BN - 1) / T::BN;
     prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     prm.wait_limit_ns = wait_limit_ns();
+    prm.o_elems = static_cast<unsigned long long>(S) * H_buf * D;
     if ((rc = device_status_ptr(&prm.status)) != H3ATTN_OK) return rc;
     const dim3 grid(static_cast<unsigned>((S + 2 * T::BM - 1) / (2 * T::BM)), static_cast<unsigned>(head_count));
     attn_fwd_kernel<D><<<grid, kAttnThreads, T::SMEM_BYTES, stream>>>(mq, mk, mv, prm);

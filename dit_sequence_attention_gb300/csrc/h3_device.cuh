@@ -29,6 +29,44 @@ __device__ __forceinline__ void record_device_error(DeviceStatus* st, int code, 
     if (atomicCAS(&st->code, 0, code) == 0) st->info = info;
 }
 
+// Kernel tags of the status info word.
+enum KernelTag : uint32_t {
+    kTagAttention = 1,
+    kTagSelftest = 2,
+    kTagQkvProj = 3,
+    kTagNormRope = 4,
+    kTagSeq2Head = 5,
+    kTagHead2Seq = 6,
+    kTagHead2SeqHeads = 7
+};
+
+// ----------------------------------------------------------------------------
+// Device index checks.  Built with H3ATTN_DEBUG_CHECKS=1 (libh3attn_debug.so),
+// every kernel checks each computed global index against the extent of its
+// buffer before the access; a failed check records H3ATTN_ERR_DEVICE_BOUNDS
+// (tag << 32 | site << 16 | low bits of the index) and the access is
+// skipped, so a wrong index shows up as a status code instead of a memory
+// fault.  In the release build the check is the constant `true`.
+// ----------------------------------------------------------------------------
+#ifndef H3ATTN_DEBUG_CHECKS
+#define H3ATTN_DEBUG_CHECKS 0
+#endif
+
+// True when [idx, idx + width) lies inside [0, extent).
+__device__ __forceinline__ bool in_bounds(DeviceStatus* st, unsigned long long idx, unsigned long long width,
+                                          unsigned long long extent, uint32_t tag, uint32_t site) {
+#if H3ATTN_DEBUG_CHECKS
+    if (idx < extent && width <= extent - idx) return true;
+    record_device_error(st, H3ATTN_ERR_DEVICE_BOUNDS,
+                        (static_cast<unsigned long long>(tag) << 32) | (static_cast<unsigned long long>(site) << 16) |
+                            (idx & 0xffffull));
+    return false;
+#else
+    (void)st; (void)idx; (void)width; (void)extent; (void)tag; (void)site;
+    return true;
+#endif
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -47,5 +47,6 @@ int launch_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, 
                         int hidden, int inner, int P, int rank, cudaStream_t stream);
 
 int launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
+int launch_selftest_bounds(void* buf, cudaStream_t stream);
 
 }  // namespace h3

@@ -114,7 +114,7 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns, DeviceStatus* 
         fence_barrier_init();
     }
     __syncthreads();
-    const WaitCtl ctl{&abort_flag, limit_ns, status, 2u};
+    const WaitCtl ctl{&abort_flag, limit_ns, status, kTagSelftest};
     if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, ctl, 1);
 }
 
@@ -176,6 +176,8 @@ extern "C" {
 
 int h3attn_version(void) { return H3ATTN_VERSION; }
 
+int h3attn_build_flags(void) { return H3ATTN_DEBUG_CHECKS ? H3ATTN_BUILD_DEBUG_CHECKS : 0; }
+
 int h3attn_last_cuda_error(void) { return t_last_cuda_error; }
 
 unsigned long long h3attn_last_device_error_info(void) { return g_last_info; }
@@ -189,6 +191,7 @@ const char* h3attn_strerror(int code) {
         case H3ATTN_ERR_CUDA: return "CUDA call failed";
         case H3ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a pipeline wait (device timeout)";
         case H3ATTN_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103";
+        case H3ATTN_ERR_DEVICE_BOUNDS: return "a kernel's index check failed and the access was skipped (debug-check build)";
         default: return "unknown status";
     }
 }
@@ -353,6 +356,15 @@ int h3attn_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
     int rc = check_device();
     if (rc != H3ATTN_OK) return rc;
     return launch_selftest_wait(limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+int h3attn_selftest_bounds(void* buf, unsigned long long bytes, void* stream) {
+    const NvtxRange nvtx_range("h3attn_selftest_bounds");
+    if (!H3ATTN_DEBUG_CHECKS) return H3ATTN_ERR_ARG;
+    if (buf == nullptr || !aligned16(buf) || bytes < 1024) return H3ATTN_ERR_ARG;
+    int rc = check_device();
+    if (rc != H3ATTN_OK) return rc;
+    return launch_selftest_bounds(buf, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -42,7 +42,9 @@ template <int D>
 __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
     const uint4* q, const uint4* k, uint4* qo, uint4* ko, float* __restrict__ dbg,
     const float* __restrict__ wq, const float* __restrict__ wk, const int32_t* __restrict__ pos, int S, int H,
-    float eps, size_t dbg_k_offset, int P, const RopeTable tab) {
+    float eps, size_t dbg_k_offset, int P, const RopeTable tab, size_t n_vec, DeviceStatus* st) {
+    // n_vec: 16-byte vectors in each of q, k, q_out, k_out (B * S * H * D / 8);
+    // st: device status word (debug-check builds).
     constexpr int VPR = D / 8;  // vectors per row
     constexpr double kTwoPi = 6.283185307179586476925286766559;
     constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
@@ -62,16 +64,18 @@ __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
 #pragma unroll
     for (int u = 0; u < kNormMaxVec; ++u) {
         const int idx = u * kNormThreads + threadIdx.x;
+        x[u] = make_uint4(0, 0, 0, 0);
         if (u < iters && idx < total) {
             const bool is_k = idx >= cpt;
-            x[u] = __ldcs((is_k ? k : q) + tok_vec + (is_k ? idx - cpt : idx));
-        } else {
-            x[u] = make_uint4(0, 0, 0, 0);
+            const size_t src = tok_vec + (is_k ? idx - cpt : idx);
+            if (in_bounds(st, src, 1, n_vec, kTagNormRope, 1)) x[u] = __ldcs((is_k ? k : q) + src);
         }
     }
     if (threadIdx.x < D / 2) {
         const int pr = threadIdx.x;
-        const double ang = static_cast<double>(__ldg(pos + 3 * s + tab.axis[pr])) * tab.inv_freq[pr];
+        const int pidx = 3 * s + tab.axis[pr];
+        const int32_t pv = in_bounds(st, pidx, 1, 3ull * S, kTagNormRope, 2) ? __ldg(pos + pidx) : 0;
+        const double ang = static_cast<double>(pv) * tab.inv_freq[pr];
         const double turns = rint(ang * kInvTwoPi);
         const float red = static_cast<float>(fma(-turns, kTwoPi, ang));
         float sn, c;
@@ -85,11 +89,11 @@ __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
 #pragma unroll
             for (int u = 0; u < kNormMaxVec; ++u) {
                 const int idx = (it0 + u) * kNormThreads + threadIdx.x;
+                x[u] = make_uint4(0, 0, 0, 0);
                 if (it0 + u < iters && idx < total) {
                     const bool is_k = idx >= cpt;
-                    x[u] = __ldcs((is_k ? k : q) + tok_vec + (is_k ? idx - cpt : idx));
-                } else {
-                    x[u] = make_uint4(0, 0, 0, 0);
+                    const size_t src = tok_vec + (is_k ? idx - cpt : idx);
+                    if (in_bounds(st, src, 1, n_vec, kTagNormRope, 3)) x[u] = __ldcs((is_k ? k : q) + src);
                 }
             }
         }
@@ -115,6 +119,7 @@ __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
             for (int off = VPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             if (!valid) continue;
             const float inv = rsqrtf(ss * inv_d + eps);
+            if (!in_bounds(st, static_cast<size_t>(part) * 8, 8, D, kTagNormRope, 4)) continue;
             const float4* wv = reinterpret_cast<const float4*>((is_k ? wk : wq) + part * 8);
             const float4 wa = __ldg(wv), wb = __ldg(wv + 1);
             const float wgt[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
@@ -140,8 +145,9 @@ __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
                 const int g = h / Hp;
                 dst = ((static_cast<size_t>(g) * S + s) * Hp + (h - g * Hp)) * VPR + part;
             }
-            __stcs((is_k ? ko : qo) + dst, out);
-            if (dbg != nullptr) {
+            if (in_bounds(st, dst, 1, n_vec, kTagNormRope, 5)) __stcs((is_k ? ko : qo) + dst, out);
+            if (dbg != nullptr &&
+                in_bounds(st, (is_k ? dbg_k_offset : 0) + (tok_vec + c) * 8, 8, 2 * dbg_k_offset, kTagNormRope, 6)) {
                 float4* d4 = reinterpret_cast<float4*>(dbg + (is_k ? dbg_k_offset : 0) + (tok_vec + c) * 8);
                 d4[0] = make_float4(y[0], y[1], y[2], y[3]);
                 d4[1] = make_float4(y[4], y[5], y[6], y[7]);
@@ -167,16 +173,20 @@ int launch_norm_rope(const void* q, const void* k, void* q_out, void* k_out, flo
         tab.axis[pr] = 0;
     }
     const size_t dbg_k = static_cast<size_t>(B) * S * H * D;
+    const size_t n_vec = dbg_k / 8;
     const unsigned blocks = static_cast<unsigned>(B) * static_cast<unsigned>(S);
     if (blocks == 0) return H3ATTN_OK;
+    DeviceStatus* st = nullptr;
+    const int rc = device_status_ptr(&st);
+    if (rc != H3ATTN_OK) return rc;
     if (D == 128)
         norm_rope_kernel<128><<<blocks, kNormThreads, 0, stream>>>(
             static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<uint4*>(q_out),
-            static_cast<uint4*>(k_out), dbg, w_q, w_k, pos, S, H, eps, dbg_k, P, tab);
+            static_cast<uint4*>(k_out), dbg, w_q, w_k, pos, S, H, eps, dbg_k, P, tab, n_vec, st);
     else
         norm_rope_kernel<64><<<blocks, kNormThreads, 0, stream>>>(
             static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<uint4*>(q_out),
-            static_cast<uint4*>(k_out), dbg, w_q, w_k, pos, S, H, eps, dbg_k, P, tab);
+            static_cast<uint4*>(k_out), dbg, w_q, w_k, pos, S, H, eps, dbg_k, P, tab, n_vec, st);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e);
 }

@@ -170,7 +170,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     cluster_sync();  // both CTAs' barriers exist before any multicast lands
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const WaitCtl ctl{abort_flag, p.wait_limit_ns, p.status, 3u};
+    const WaitCtl ctl{abort_flag, p.wait_limit_ns, p.status, kTagQkvProj};
     const uint32_t sA = sbase + T::OFF_A, sB = sbase + T::OFF_B;
 
     if (warp == 0) {
@@ -249,7 +249,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             for (int c = 0; c < T::BN / 32; ++c) {
                 float a[32];
                 tmem_ld32(lane_addr + acc * T::ACC_COLS + 32 * c, a);
-                if (row < p.S && 32 * c < cols) {
+                if (row < p.S && 32 * c < cols &&
+                    in_bounds(p.status, static_cast<size_t>(row) * p.Nr + ntile * T::BN + 32 * c,
+                              8ull * min(4, (cols - 32 * c) / 8), static_cast<unsigned long long>(p.S) * p.Nr,
+                              kTagQkvProj, 1)) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
                     const int nv = min(4, (cols - 32 * c) / 8);
 #pragma unroll

@@ -47,8 +47,13 @@ enum h3attn_status {
     H3ATTN_ERR_ALIAS = -3,          /* output overlaps an input where that is not allowed */
     H3ATTN_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed (see h3attn_last_cuda_error) */
     H3ATTN_ERR_DEVICE_TIMEOUT = -5, /* a kernel gave up on a pipeline wait (device status word) */
-    H3ATTN_ERR_UNSUPPORTED_DEVICE = -6 /* current device is not an sm_103 (GB300-class) GPU */
+    H3ATTN_ERR_UNSUPPORTED_DEVICE = -6, /* current device is not an sm_103 (GB300-class) GPU */
+    H3ATTN_ERR_DEVICE_BOUNDS = -7   /* debug-check builds: a kernel computed an index outside its buffer
+                                       and skipped that access (device status word) */
 };
+
+/* Bits of h3attn_build_flags(). */
+#define H3ATTN_BUILD_DEBUG_CHECKS 1 /* kernels check every computed global index before the access */
 
 /*
  * h3attn_qk_norm_rope -- fused QK-RMSNorm and three-axis rotary embedding.
@@ -179,13 +184,18 @@ H3ATTN_API int h3attn_qkv_proj_fp8(const void* x, const void* w, float scale, vo
  * h3attn_get_device_status -- synchronise `stream`, then read and clear the
  * device status word of the current device.  Returns H3ATTN_OK,
  * H3ATTN_ERR_DEVICE_TIMEOUT (a kernel gave up on a wait, wrote nothing
- * trustworthy and returned), or H3ATTN_ERR_CUDA if the synchronisation itself
- * failed.
+ * trustworthy and returned), H3ATTN_ERR_DEVICE_BOUNDS (debug-check builds
+ * only: a kernel's index check failed and the access was skipped), or
+ * H3ATTN_ERR_CUDA if the synchronisation itself failed.  The first error
+ * recorded since the last read wins.
  */
 H3ATTN_API int h3attn_get_device_status(void* stream);
 
-/* Diagnostic word recorded with the last device error (kernel tag << 32 |
- * wait site << 16 | block index), 0 if none.  Read after h3attn_get_device_status. */
+/* Diagnostic word recorded with the last device error, 0 if none; read after
+ * h3attn_get_device_status.  Kernel tag << 32 | site << 16 | low 16 bits of
+ * the block index (timeouts) or of the offending index (bounds checks).
+ * Kernel tags: 1 attention, 2 wait self-test, 3 fp8 projection,
+ * 4 norm/RoPE, 5 seq2head, 6 head2seq, 7 head2seq_heads. */
 H3ATTN_API unsigned long long h3attn_last_device_error_info(void);
 
 /* cudaError_t value behind the most recent H3ATTN_ERR_CUDA on this thread. */
@@ -197,6 +207,10 @@ H3ATTN_API const char* h3attn_strerror(int code);
 /* H3ATTN_VERSION of the built library. */
 H3ATTN_API int h3attn_version(void);
 
+/* H3ATTN_BUILD_* bits the library was compiled with (0 for the release build;
+ * H3ATTN_BUILD_DEBUG_CHECKS for libh3attn_debug.so). */
+H3ATTN_API int h3attn_build_flags(void);
+
 /*
  * h3attn_selftest_wait_timeout -- failure-detection self-test.  Launches one
  * block whose wait on an mbarrier that nothing ever arrives on uses the same
@@ -206,6 +220,22 @@ H3ATTN_API int h3attn_version(void);
  * reports it and the context stays usable.
  */
 H3ATTN_API int h3attn_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
+/*
+ * h3attn_selftest_bounds -- self-test of the device index checks of a
+ * debug-check build.  Runs the seq2head kernel on a tiny case (S = 2, H = 2,
+ * D = 64, P = 2: 512 bytes in, 512 bytes out, both inside `buf`) while telling
+ * the kernel that its output is one 16-byte vector shorter than it is, so the
+ * kernel's own check must refuse the last store: it records
+ * H3ATTN_ERR_DEVICE_BOUNDS (tag 5) and skips it.  Every access the kernel
+ * makes, refused or not, lies inside `buf`.
+ * `buf`: device memory owned by the caller, 16-byte aligned, >= 1024 bytes
+ * (contents overwritten).  Asynchronous on `stream`; read the outcome with
+ * h3attn_get_device_status().  Returns H3ATTN_ERR_ARG without launching in a
+ * build without H3ATTN_BUILD_DEBUG_CHECKS, or for a null, misaligned or too
+ * small buffer.
+ */
+H3ATTN_API int h3attn_selftest_bounds(void* buf, unsigned long long bytes, void* stream);
 
 #ifdef __cplusplus
 }

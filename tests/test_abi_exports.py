@@ -52,7 +52,44 @@ def test_version_and_strerror_need_no_gpu(lib):
     assert lib.h3attn_version() == 1
     assert lib.h3attn_strerror(0) == b"ok"
     assert b"timeout" in lib.h3attn_strerror(-5)
+    assert b"index check" in lib.h3attn_strerror(-7)
     assert lib.h3attn_strerror(12345) == b"unknown status"
+
+
+@pytest.fixture(scope="module")
+def debug_lib():
+    from dit_sequence_attention_gb300 import build
+    path = build.build(debug=True)
+    import dit_sequence_attention_gb300 as h3
+    dl = ctypes.CDLL(path)
+    for name, (res, args) in h3.SIGNATURES.items():
+        getattr(dl, name).restype = res
+        getattr(dl, name).argtypes = args
+    return dl
+
+
+def test_build_flags_tell_the_two_builds_apart(lib, debug_lib):
+    import dit_sequence_attention_gb300 as h3
+    assert lib.h3attn_build_flags() == 0
+    assert debug_lib.h3attn_build_flags() == h3.H3ATTN_BUILD_DEBUG_CHECKS
+
+
+def test_debug_build_exports_the_same_symbols(debug_lib):
+    import subprocess
+    from dit_sequence_attention_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB_DEBUG], capture_output=True, text=True).stdout
+    assert set(re.findall(r"\b(h3attn_\w+)$", out, flags=re.M)) == set(declared_functions())
+
+
+def test_bounds_selftest_refuses_without_checks_or_buffer(lib, debug_lib):
+    import dit_sequence_attention_gb300 as h3
+    fake = 0x10000000
+    # the release build has no checks to test: refused before any CUDA call
+    assert lib.h3attn_selftest_bounds(fake, 4096, None) == h3.H3ATTN_ERR_ARG
+    # the debug build refuses a null, misaligned or too small buffer before any CUDA call
+    assert debug_lib.h3attn_selftest_bounds(None, 4096, None) == h3.H3ATTN_ERR_ARG
+    assert debug_lib.h3attn_selftest_bounds(fake + 8, 4096, None) == h3.H3ATTN_ERR_ARG
+    assert debug_lib.h3attn_selftest_bounds(fake, 1008, None) == h3.H3ATTN_ERR_ARG
 
 
 def test_argument_checks_run_before_any_cuda_call(lib):
@@ -97,7 +134,10 @@ def test_argument_checks_run_before_any_cuda_call(lib):
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     import dit_sequence_attention_gb300 as h3
-    monkeypatch.setattr(h3, "_lib", None)
-    monkeypatch.setattr(h3, "_LIB_PATH", str(tmp_path / "missing.so"))
-    with pytest.raises(RuntimeError, match="not built"):
-        h3.load_library()
+    missing = str(tmp_path / "missing.so")
+    monkeypatch.setattr(h3, "_libs", {})
+    monkeypatch.setattr(h3, "_LIB_PATHS", {False: missing, True: missing})
+    for debug in (False, True):
+        monkeypatch.setattr(h3, "_debug", debug)
+        with pytest.raises(RuntimeError, match="not built"):
+            h3.load_library()
