@@ -146,6 +146,32 @@ def test_attention_matches_oracle(h3, cuda_device, S, H, D, kv):
     assert np.all(err <= ATTN_TOL), f"per-head rel err {err}"
 
 
+@pytest.mark.parametrize("log2_growth_per_tile", [12.0, 6.0, -4.0])
+def test_attention_running_max_growth(h3, cuda_device, log2_growth_per_tile):
+    """Scores that climb (or fall) from one 128-key tile to the next, so the
+    kernel's running row max grows by ~12 (O rescaled at every tile), ~6 (rescaled
+    every other tile; in between the stale max is kept and P reaches 2^6) or
+    falls (never rescaled).  N(0,1) inputs almost never take these paths."""
+    S, H, D, kv = 1024, 2, 128, 1000
+    g = torch.Generator().manual_seed(77)
+    u = torch.randn(H, D, generator=g)
+    u = u / u.norm(dim=-1, keepdim=True) * D ** 0.5             # |u|^2 = D per head
+    # score(i, j) ~ a_j * |u|^2 / sqrt(D) = a_j * sqrt(D); in log2 units x log2(e)
+    rate = log2_growth_per_tile / (D ** 0.5 * 1.4426950408889634)  # growth of a per 128 keys
+    a = rate * torch.arange(S, dtype=torch.float32) / 128.0
+    if log2_growth_per_tile < 0:
+        a = a - a[kv - 1]                                          # falling, ending near 0
+    q = (u[None] + 0.1 * torch.randn(S, H, D, generator=g)).to(torch.bfloat16)
+    k = (a[:, None, None] * u[None] + 0.1 * torch.randn(S, H, D, generator=g)).to(torch.bfloat16)
+    v = torch.randn(S, H, D, generator=g).to(torch.bfloat16)
+    o = torch.empty((S, H, D), dtype=torch.bfloat16, device=cuda_device)
+    h3.h3attn_forward(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device), o, kv_len=kv)
+    assert h3.h3attn_get_device_status() == 0
+    ref = oracle.attention(oracle.bf16_to_f64(q), oracle.bf16_to_f64(k), oracle.bf16_to_f64(v), kv_len=kv)
+    err = per_head_rel_err(o.float().cpu().numpy(), ref)
+    assert np.all(err <= ATTN_TOL), f"per-head rel err {err}"
+
+
 def test_attention_c2_workload_sampled_rows(h3, cuda_device):
     w = synth.WORKLOADS["c2"]
     rng = np.random.default_rng(3)
