@@ -59,8 +59,11 @@ def parse_args():
     return ap.parse_args()
 
 
-def load_peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def load_peaks(path=None):
+    """Roofline denominators: the measured peaks file when present (flat or
+    nested JSON with hbm_gbs / bf16_tflops / bf16_tflops_sustained), else the
+    fallback figures.  Returns (peaks, "measured" | "fallback")."""
+    path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         try:
             with open(path) as f:
