@@ -41,6 +41,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("attention TFLOPS & tokens/s at 56 heads×128, 50k-262k tokens; % of bf16 peak")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HBM_SPEC_GBS = 7900.0            # HBM3e spec-sheet bandwidth, reported beside the measured copy figure
+BF16_FLOP_PER_CLK_SM = 8192.0    # dense bf16 tcgen05 rate per SM per clock (M128 N128 K16 in 64 cycles)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_dram_traffic.txt")
 
 
@@ -377,6 +379,9 @@ def main():
     hbm_peak = peaks["hbm_gbs"]
     for kname in ("qk_norm_rope_seq2head", "seq2head_v", "head2seq"):
         kernels[kname]["frac_of_hbm_peak"] = kernels[kname]["GB_per_s"] / hbm_peak
+        kernels[kname]["frac_of_hbm_spec"] = kernels[kname]["GB_per_s"] / HBM_SPEC_GBS
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    clock_peak = (n_sm * BF16_FLOP_PER_CLK_SM * clk["sm_mhz"] * 1e6 / 1e12) if clk else None
 
     # ---------------------------------------------------------------- e2e
     # Through the public API from pinned host buffers: every step copies its
@@ -482,12 +487,16 @@ def main():
         "config": workload_config(w, P),
         "tokens_per_s": w.S_v * args.steps * world / (elapsed_ms * 1e-3),
         "frac_of_bf16_peak": value / peak,
+        "padded_work_tflops": value * S / w.S_v,
+        "padded_work_note": "the same step counted as 4*S*S_v*D*H (every padded query row against the valid keys)",
         "roofline": {"kernel": "attn_fwd_kernel<128> (one 28-head group launch)" if D == 128 else "attn_fwd_kernel",
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16 dense, sustained",
                      "burst_peak": peaks["bf16_tflops"], "frac_of_burst": achieved / peaks["bf16_tflops"],
-                     "algorithmic_flops_per_launch": flops_launch},
+                     "algorithmic_flops_per_launch": flops_launch,
+                     "tensor_peak_at_median_clock": clock_peak,
+                     "frac_of_tensor_peak_at_median_clock": (achieved / clock_peak) if clock_peak else None},
         "kernels": kernels,
         "hbm_peak_GB_per_s": hbm_peak,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
