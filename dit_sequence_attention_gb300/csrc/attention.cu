@@ -7,10 +7,15 @@
 //
 // How (one CTA = one head x 256 query rows, 320 threads):
 //   warp 8      TMA producer: Q tiles once, then K/V tiles of 128 keys into a
-//               two-stage ring per operand (128B-swizzled boxes of 64 columns).
+//               three-stage key ring and a two-stage value ring (128B-swizzled
+//               boxes of 64 columns).
 //   warp 9      allocates 512 TMEM columns, one lane issues every tcgen05.mma:
 //               S_i = Q_i K^T (both operands in shared memory) and
 //               O_i += P_i V   (P from TMEM, V from shared memory, MN-major).
+//               A thread that waits on an mbarrier lets the MMAs it has queued
+//               drain, so its only waits between MMA groups are those for P;
+//               the TMA barriers of a step are waited after the last group of
+//               the step before.
 //   warps 0-3   softmax for query tile 0 (rows 0..127), warps 4-7 for tile 1.
 //               Thread = one query row = one TMEM lane: the 128 scores arrive in
 //               one 128-column TMEM load; row max with three-input max; then the
