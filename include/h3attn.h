@@ -20,7 +20,8 @@
  *  - Return value: H3ATTN_OK (0) or a negative H3ATTN_ERR_* code.  Arguments
  *    are checked on the host before anything is launched; a rejected call
  *    enqueues nothing.  No call traps or aborts the process.
- *  - Device errors (a pipeline wait that ran out of time) are recorded in a
+ *  - Device errors (a pipeline wait that ran out of time; in the debug-check
+ *    build libh3attn_debug.so, an index check that failed) are recorded in a
  *    device status word and reported by h3attn_get_device_status().
  */
 #ifndef H3ATTN_H
