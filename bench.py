@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-proj", action="store_true", help="skip timing the all-gather variant's fp8 projection")
+    ap.add_argument("--no-chunks", action="store_true",
+                    help="skip timing the step with head-chunked attention and overlapped output exchange")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
 
@@ -443,6 +445,41 @@ def main():
     h2d = 3 * tensor_bytes + hpos.numel() * 4
     d2h = tensor_bytes
 
+    # ------------------------------- head-chunked attention, overlapped exchange
+    # The same step with each group's heads split into chunks; the output
+    # exchange of chunk c runs on a second stream while attention computes
+    # chunk c+1 (bit-identical output for any chunk count).
+    chunk_runs = None
+    if not args.no_chunks:
+        xs = torch.cuda.Stream(dev)
+        chunk_runs = {"chunks": [1], "ms_per_step": [ms_step], "attention_launches_per_step": [P]}
+        ref_out = h3.ulysses_attention_step(q, k, v, wq, wk, pos, P, w.S_v, *w.rope_split, w.eps, w.theta,
+                                            work=work, stream=stream).clone()
+        for c in (2, 4):
+            def chunked_step():
+                return h3.ulysses_attention_step(q, k, v, wq, wk, pos, P, w.S_v, *w.rope_split, w.eps, w.theta,
+                                                  work=work, stream=stream, attn_chunks=c, exchange_stream=xs)
+            for _ in range(2):
+                chunked_step()
+            torch.cuda.synchronize(dev)
+            ca, cb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n_c = max(3, min(args.steps, 6))
+            ca.record(stream)
+            for _ in range(n_c):
+                out_c = chunked_step()
+            cb.record(stream)  # the step joins the exchange stream back into `stream` before returning
+            torch.cuda.synchronize(dev)
+            if h3.h3attn_get_device_status() != 0:
+                raise RuntimeError("device status error in the chunked step")
+            if not torch.equal(out_c.view(torch.int16), ref_out.view(torch.int16)):
+                raise RuntimeError(f"chunked step ({c} chunks) is not bit-identical to the unchunked one")
+            chunk_runs["chunks"].append(c)
+            chunk_runs["ms_per_step"].append(ca.elapsed_time(cb) / n_c)
+            chunk_runs["attention_launches_per_step"].append(P * c)
+        chunk_runs["note"] = ("whole step; output exchange of each head chunk on a second stream, overlapping the "
+                              "next chunk's attention; outputs checked bit-identical to the unchunked step")
+        del ref_out
+
     # ---------------------------------------------- all-gather variant projection
     proj = None
     if not args.no_proj and D == 128:
@@ -507,6 +544,7 @@ def main():
         "clocks": clk,
         "cpu_baseline": cpu,
         "ag_qkv_proj_fp8": proj,
+        "head_chunk_overlap": chunk_runs,
     }
     print(json.dumps(line), flush=True)
 
