@@ -102,10 +102,16 @@ def load_library():
     return lib
 
 
-def _stream_ptr(stream) -> int:
+def _stream_ptr(stream, device=None) -> int:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return int(stream.cuda_stream)
+
+
+def _on(t: torch.Tensor):
+    """Make the tensors' GPU the current device for the call: the library
+    launches on the current device and refuses memory of any other."""
+    return torch.cuda.device(t.device)
 
 
 def _check(fn: str, rc: int):
@@ -156,9 +162,10 @@ def h3attn_qk_norm_rope(q, k, q_out, k_out, w_q, w_k, pos, d_t, d_h, d_w, eps=1e
         if dbg_fp32.dtype != torch.float32 or dbg_fp32.numel() != 2 * B * S * H * D or not dbg_fp32.is_contiguous():
             raise ValueError("dbg_fp32 must be a contiguous fp32 tensor of 2*B*S*H*D elements")
         dbg = dbg_fp32.data_ptr()
-    rc = lib.h3attn_qk_norm_rope(q.data_ptr(), k.data_ptr(), q_out.data_ptr(), k_out.data_ptr(), dbg,
-                                 w_q.data_ptr(), w_k.data_ptr(), pos.data_ptr(), B, S, H, D, d_t, d_h, d_w,
-                                 float(eps), float(theta), _stream_ptr(stream))
+    with _on(q):
+        rc = lib.h3attn_qk_norm_rope(q.data_ptr(), k.data_ptr(), q_out.data_ptr(), k_out.data_ptr(), dbg,
+                                     w_q.data_ptr(), w_k.data_ptr(), pos.data_ptr(), B, S, H, D, d_t, d_h, d_w,
+                                     float(eps), float(theta), _stream_ptr(stream, q.device))
     _check("h3attn_qk_norm_rope", rc)
 
 
@@ -186,9 +193,10 @@ def h3attn_qk_norm_rope_seq2head(q, k, qh_out, kh_out, w_q, w_k, pos, P, d_t, d_
         if dbg_fp32.dtype != torch.float32 or dbg_fp32.numel() != 2 * S * H * D or not dbg_fp32.is_contiguous():
             raise ValueError("dbg_fp32 must be a contiguous fp32 tensor of 2*S*H*D elements")
         dbg = dbg_fp32.data_ptr()
-    rc = lib.h3attn_qk_norm_rope_seq2head(q.data_ptr(), k.data_ptr(), qh_out.data_ptr(), kh_out.data_ptr(), dbg,
-                                          w_q.data_ptr(), w_k.data_ptr(), pos.data_ptr(), S, H, D, int(P), d_t, d_h,
-                                          d_w, float(eps), float(theta), _stream_ptr(stream))
+    with _on(q):
+        rc = lib.h3attn_qk_norm_rope_seq2head(q.data_ptr(), k.data_ptr(), qh_out.data_ptr(), kh_out.data_ptr(), dbg,
+                                              w_q.data_ptr(), w_k.data_ptr(), pos.data_ptr(), S, H, D, int(P), d_t,
+                                              d_h, d_w, float(eps), float(theta), _stream_ptr(stream, q.device))
     _check("h3attn_qk_norm_rope_seq2head", rc)
 
 
@@ -212,10 +220,11 @@ def h3attn_forward(q, k, v, o, head_begin=0, head_count=None, kv_len=None, scale
         if len(vals) != B:
             raise ValueError(f"kv_len has {len(vals)} entries, expected {B}")
         kv_arr = (ctypes.c_int32 * B)(*vals)
-    rc = lib.h3attn_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, S, H, D,
-                            int(head_begin), int(head_count),
-                            ctypes.cast(kv_arr, ctypes.c_void_p) if kv_arr is not None else None,
-                            float(scale), _stream_ptr(stream))
+    with _on(q):
+        rc = lib.h3attn_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, S, H, D,
+                                int(head_begin), int(head_count),
+                                ctypes.cast(kv_arr, ctypes.c_void_p) if kv_arr is not None else None,
+                                float(scale), _stream_ptr(stream, q.device))
     _check("h3attn_forward", rc)
 
 
@@ -225,7 +234,8 @@ def _layout(fn_name, src, dst, S, H, D, P, stream):
     _bf16(dst, "out", src.device)
     if src.numel() != S * H * D or dst.numel() != S * H * D:
         raise ValueError("in/out must hold S*H*D elements")
-    rc = getattr(lib, fn_name)(src.data_ptr(), dst.data_ptr(), S, H, D, int(P), _stream_ptr(stream))
+    with _on(src):
+        rc = getattr(lib, fn_name)(src.data_ptr(), dst.data_ptr(), S, H, D, int(P), _stream_ptr(stream, src.device))
     _check(fn_name, rc)
 
 
@@ -255,8 +265,9 @@ def h3attn_head2seq_heads(x_group, out, P, group, head_begin, head_count, stream
     S, Hp, D = x_group.shape
     if tuple(out.shape) != (S, Hp * P, D):
         raise ValueError("out must be [S, H, D] with H = P * (H/P)")
-    rc = lib.h3attn_head2seq_heads(x_group.data_ptr(), out.data_ptr(), S, Hp * P, D, int(P), int(group),
-                                   int(head_begin), int(head_count), _stream_ptr(stream))
+    with _on(x_group):
+        rc = lib.h3attn_head2seq_heads(x_group.data_ptr(), out.data_ptr(), S, Hp * P, D, int(P), int(group),
+                                       int(head_begin), int(head_count), _stream_ptr(stream, x_group.device))
     _check("h3attn_head2seq_heads", rc)
 
 
@@ -278,9 +289,10 @@ def h3attn_qkv_proj_fp8(x_fp8, w_fp8, scale, q_out, k_out, v_out, P, rank, strea
         _bf16(t, n, x_fp8.device)
         if t.numel() != S * (inner // P):
             raise ValueError(f"{n} must hold S * inner/P = {S * (inner // P)} elements")
-    rc = lib.h3attn_qkv_proj_fp8(x_fp8.data_ptr(), w_fp8.data_ptr(), float(scale), q_out.data_ptr(),
-                                 k_out.data_ptr(), v_out.data_ptr(), S, hidden, inner, int(P), int(rank),
-                                 _stream_ptr(stream))
+    with _on(x_fp8):
+        rc = lib.h3attn_qkv_proj_fp8(x_fp8.data_ptr(), w_fp8.data_ptr(), float(scale), q_out.data_ptr(),
+                                     k_out.data_ptr(), v_out.data_ptr(), S, hidden, inner, int(P), int(rank),
+                                     _stream_ptr(stream, x_fp8.device))
     _check("h3attn_qkv_proj_fp8", rc)
 
 
@@ -308,7 +320,9 @@ def h3attn_selftest_bounds(buf: torch.Tensor, stream=None):
     ``h3attn_get_device_status()`` (H3ATTN_ERR_DEVICE_BOUNDS expected)."""
     if not isinstance(buf, torch.Tensor) or not buf.is_cuda or not buf.is_contiguous():
         raise ValueError("buf must be a contiguous CUDA tensor")
-    rc = load_library().h3attn_selftest_bounds(buf.data_ptr(), buf.numel() * buf.element_size(), _stream_ptr(stream))
+    with _on(buf):
+        rc = load_library().h3attn_selftest_bounds(buf.data_ptr(), buf.numel() * buf.element_size(),
+                                                   _stream_ptr(stream, buf.device))
     _check("h3attn_selftest_bounds", rc)
 
 

@@ -10,6 +10,7 @@
 #include <cstdlib>
 #include <cmath>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "h3_device.cuh"
@@ -138,8 +139,12 @@ static bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 // The kernels are built for sm_103a only; refuse anything else up front so a
-// wrong device fails with a clear code instead of a launch error.
-static int check_device() {
+// wrong device fails with a clear code instead of a launch error.  Then every
+// buffer pointer must be memory the current device's kernels can address:
+// device memory of this device, or managed memory.  A host pointer, or
+// device memory of another GPU, is refused with H3ATTN_ERR_ARG before
+// anything is launched (null entries are optional buffers and are skipped).
+static int check_device(std::initializer_list<const void*> ptrs = {}) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -147,6 +152,17 @@ static int check_device() {
     if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return cuda_fail(e);
     if (major != 10 || minor != 3) return H3ATTN_ERR_UNSUPPORTED_DEVICE;
+    for (const void* p : ptrs) {
+        if (p == nullptr) continue;
+        cudaPointerAttributes a;
+        e = cudaPointerGetAttributes(&a, p);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();  // an unknown pointer is an argument error, not a sticky CUDA error
+            return H3ATTN_ERR_ARG;
+        }
+        if (a.type == cudaMemoryTypeManaged) continue;
+        if (a.type != cudaMemoryTypeDevice || a.device != dev) return H3ATTN_ERR_ARG;
+    }
     return H3ATTN_OK;
 }
 
@@ -215,7 +231,7 @@ int h3attn_qk_norm_rope(const void* q, const void* k, void* q_out, void* k_out, 
     if (overlap(q_out, bytes, k, bytes) || overlap(k_out, bytes, q, bytes)) return H3ATTN_ERR_ALIAS;
     if (dbg_fp32 && (overlap(dbg_fp32, bytes * 4, q_out, bytes) || overlap(dbg_fp32, bytes * 4, k_out, bytes)))
         return H3ATTN_ERR_ALIAS;
-    int rc = check_device();
+    int rc = check_device({q, k, q_out, k_out, dbg_fp32, w_q, w_k, pos});
     if (rc != H3ATTN_OK) return rc;
     return launch_norm_rope(q, k, q_out, k_out, dbg_fp32, w_q, w_k, pos, B, S, H, D, d_t, d_h, d_w, eps,
                             static_cast<double>(theta), 1, static_cast<cudaStream_t>(stream));
@@ -240,7 +256,7 @@ int h3attn_qk_norm_rope_seq2head(const void* q, const void* k, void* qh_out, voi
         return H3ATTN_ERR_ALIAS;
     if (dbg_fp32 && (overlap(dbg_fp32, bytes * 4, qh_out, bytes) || overlap(dbg_fp32, bytes * 4, kh_out, bytes)))
         return H3ATTN_ERR_ALIAS;
-    int rc = check_device();
+    int rc = check_device({q, k, qh_out, kh_out, dbg_fp32, w_q, w_k, pos});
     if (rc != H3ATTN_OK) return rc;
     return launch_norm_rope(q, k, qh_out, kh_out, dbg_fp32, w_q, w_k, pos, 1, S, H, D, d_t, d_h, d_w, eps,
                             static_cast<double>(theta), P, static_cast<cudaStream_t>(stream));
@@ -262,7 +278,7 @@ int h3attn_forward(const void* q, const void* k, const void* v, void* o, int B, 
     const size_t bytes = item * B;
     if (overlap(o, bytes, q, bytes) || overlap(o, bytes, k, bytes) || overlap(o, bytes, v, bytes))
         return H3ATTN_ERR_ALIAS;
-    int rc = check_device();
+    int rc = check_device({q, k, v, o});
     if (rc != H3ATTN_OK) return rc;
     const float sc = scale > 0.0f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
     for (int b = 0; b < B; ++b) {
@@ -280,7 +296,7 @@ int h3attn_seq2head(const void* in, void* out, int S, int H, int D, int P, void*
     const NvtxRange nvtx_range("h3attn_seq2head");
     int rc = check_layout_args(in, out, S, H, D, P);
     if (rc != H3ATTN_OK) return rc;
-    if ((rc = check_device()) != H3ATTN_OK) return rc;
+    if ((rc = check_device({in, out})) != H3ATTN_OK) return rc;
     return launch_seq2head(in, out, S, H, D, P, static_cast<cudaStream_t>(stream));
 }
 
@@ -288,7 +304,7 @@ int h3attn_head2seq(const void* in, void* out, int S, int H, int D, int P, void*
     const NvtxRange nvtx_range("h3attn_head2seq");
     int rc = check_layout_args(in, out, S, H, D, P);
     if (rc != H3ATTN_OK) return rc;
-    if ((rc = check_device()) != H3ATTN_OK) return rc;
+    if ((rc = check_device({in, out})) != H3ATTN_OK) return rc;
     return launch_head2seq(in, out, S, H, D, P, static_cast<cudaStream_t>(stream));
 }
 
@@ -305,7 +321,7 @@ int h3attn_head2seq_heads(const void* in_group, void* out, int S, int H, int D, 
     if (elems / 8 >= (1ull << 32)) return H3ATTN_ERR_SHAPE;
     const size_t in_bytes = static_cast<size_t>(S) * Hp * D * 2;
     if (overlap(in_group, in_bytes, out, elems * 2)) return H3ATTN_ERR_ALIAS;
-    int rc = check_device();
+    int rc = check_device({in_group, out});
     if (rc != H3ATTN_OK) return rc;
     return launch_head2seq_heads(in_group, out, S, H, D, P, group, head_begin, head_count,
                                  static_cast<cudaStream_t>(stream));
@@ -328,7 +344,7 @@ int h3attn_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, 
         for (int j = i + 1; j < 3; ++j)
             if (overlap(outs[i], ob, outs[j], ob)) return H3ATTN_ERR_ALIAS;
     }
-    int rc = check_device();
+    int rc = check_device({x, w, q_out, k_out, v_out});
     if (rc != H3ATTN_OK) return rc;
     return launch_qkv_proj_fp8(x, w, scale, q_out, k_out, v_out, S, hidden, inner, P, rank,
                                static_cast<cudaStream_t>(stream));
@@ -362,7 +378,7 @@ int h3attn_selftest_bounds(void* buf, unsigned long long bytes, void* stream) {
     const NvtxRange nvtx_range("h3attn_selftest_bounds");
     if (!H3ATTN_DEBUG_CHECKS) return H3ATTN_ERR_ARG;
     if (buf == nullptr || !aligned16(buf) || bytes < 1024) return H3ATTN_ERR_ARG;
-    int rc = check_device();
+    int rc = check_device({buf});
     if (rc != H3ATTN_OK) return rc;
     return launch_selftest_bounds(buf, static_cast<cudaStream_t>(stream));
 }

@@ -12,8 +12,10 @@
  *    64 or 128; the head count is a runtime value, which is how a caller hands
  *    the kernel a buffer that holds only 56/P heads (the diffusers TP PR
  *    reshapes attention by the fixed head_dim and lets the head count follow).
- *  - Every tensor pointer is a DEVICE pointer, 16-byte aligned.  The caller
- *    owns all buffers; the library allocates no device memory per call.
+ *  - Every tensor pointer is a DEVICE pointer of the current device (or
+ *    managed memory), 16-byte aligned; anything else (a host pointer, memory
+ *    of another GPU) is refused with H3ATTN_ERR_ARG before any launch.  The
+ *    caller owns all buffers; the library allocates no device memory per call.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls only enqueue work and return; nothing synchronises except
  *    h3attn_get_device_status().

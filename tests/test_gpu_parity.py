@@ -231,6 +231,29 @@ def test_attention_argument_errors(h3, cuda_device):
     assert e.value.code == h3.H3ATTN_ERR_ALIAS
 
 
+def test_host_memory_is_refused_before_any_launch(h3, cuda_device):
+    """Every call checks that its buffers are memory of the current device:
+    host memory (pinned or pageable) is refused with H3ATTN_ERR_ARG and
+    nothing is launched (the device status stays clean)."""
+    lib = h3.load_library()
+    S, H, D = 256, 4, 64
+    dev_buf = torch.zeros((S, H, D), dtype=torch.bfloat16, device=cuda_device)
+    out = torch.zeros_like(dev_buf)
+    pinned = torch.zeros((S, H, D), dtype=torch.bfloat16).pin_memory()
+    pageable = torch.zeros((S, H, D), dtype=torch.bfloat16)
+    st = torch.cuda.current_stream(cuda_device).cuda_stream
+    for host in (pinned, pageable):
+        assert lib.h3attn_forward(host.data_ptr(), dev_buf.data_ptr(), dev_buf.data_ptr(), out.data_ptr(),
+                                  1, S, H, D, 0, H, None, 0.0, st) == h3.H3ATTN_ERR_ARG
+        assert lib.h3attn_seq2head(dev_buf.data_ptr(), host.data_ptr(), S, H, D, 2, st) == h3.H3ATTN_ERR_ARG
+        assert lib.h3attn_head2seq(host.data_ptr(), out.data_ptr(), S, H, D, 2, st) == h3.H3ATTN_ERR_ARG
+    assert h3.h3attn_get_device_status() == 0
+    assert bool((out == 0).all())
+    # device memory of the current device passes the same check
+    assert lib.h3attn_seq2head(dev_buf.data_ptr(), out.data_ptr(), S, H, D, 2, st) == h3.H3ATTN_OK
+    assert h3.h3attn_get_device_status() == 0
+
+
 # ------------------------------------------------------------- whole path
 @pytest.mark.parametrize("P", [1, 2, 4])
 def test_pipeline_c2_matches_oracle(h3, cuda_device, P):
