@@ -57,6 +57,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-proj", action="store_true", help="skip timing the all-gather variant's fp8 projection")
+    ap.add_argument("--no-graph", action="store_true", help="skip timing the step replayed as a CUDA graph")
     ap.add_argument("--no-chunks", action="store_true",
                     help="skip timing the step with head-chunked attention and overlapped output exchange")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -480,6 +481,51 @@ def main():
                               "next chunk's attention; outputs checked bit-identical to the unchunked step")
         del ref_out
 
+    # ------------------------------------------------ whole step as a CUDA graph
+    # One graph launch per step instead of five library calls: no per-call host
+    # work.  Timed at the bench workload and at c2 (4,096 tokens), where the
+    # host side of eager calls is a visible share of the step.
+    graph_runs = None
+    if not args.no_graph and D == 128:
+        graph_runs = {}
+        for wname in dict.fromkeys((w.name, "c2")):
+            ww = synth.WORKLOADS[wname]
+            if wname == w.name:
+                gq, gk, gv, gpos = q, k, v, pos
+            else:
+                gq, gk, gv = (synth.randn_bf16((ww.S, ww.H, ww.D), 500 + i, dev, zero_rows_from=ww.S_v)
+                              for i in range(3))
+                gpos = torch.from_numpy(synth.packed_positions(ww)).to(dev)
+            gargs = (P, ww.S_v, *ww.rope_split, ww.eps, ww.theta)
+            sg = h3.StepGraph(gq, gk, gv, wq, wk, gpos, *gargs)
+            gwork = h3.make_workspace(ww.S, ww.H, ww.D, P, dev)
+            n_g = max(3, min(args.steps, 20)) if wname == w.name else 200
+
+            def timed(fn, n):
+                for _ in range(3):
+                    fn()
+                torch.cuda.synchronize(dev)
+                ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ga.record(stream)
+                for _ in range(n):
+                    fn()
+                gb.record(stream)
+                torch.cuda.synchronize(dev)
+                return ga.elapsed_time(gb) / n
+
+            eager_ms = timed(lambda: h3.ulysses_attention_step(gq, gk, gv, wq, wk, gpos, *gargs, work=gwork,
+                                                               stream=stream), n_g)
+            graph_ms = timed(sg.replay, n_g)
+            if h3.h3attn_get_device_status() != 0:
+                raise RuntimeError("device status error in the graph timing")
+            if not torch.equal(sg.out.view(torch.int16), gwork["o"].view(torch.int16)):
+                raise RuntimeError(f"graph replay differs from the eager step ({wname})")
+            graph_runs[wname] = {"tokens": ww.S, "eager_ms_per_step": eager_ms, "graph_ms_per_step": graph_ms,
+                                 "steps": n_g}
+            del sg, gwork
+        graph_runs["note"] = ("StepGraph: the whole step captured once, replayed with one graph launch; "
+                              "outputs checked bit-identical to the eager step")
+
     # ---------------------------------------------- all-gather variant projection
     proj = None
     if not args.no_proj and D == 128:
@@ -545,6 +591,7 @@ def main():
         "cpu_baseline": cpu,
         "ag_qkv_proj_fp8": proj,
         "head_chunk_overlap": chunk_runs,
+        "cuda_graph": graph_runs,
     }
     print(json.dumps(line), flush=True)
 

@@ -25,7 +25,7 @@ __all__ = [
     "h3attn_head2seq", "h3attn_head2seq_heads", "h3attn_qkv_proj_fp8",
     "h3attn_get_device_status", "h3attn_strerror", "h3attn_version", "h3attn_selftest_wait_timeout",
     "h3attn_last_device_error_info", "h3attn_build_flags", "h3attn_selftest_bounds", "use_debug_checks",
-    "ulysses_attention_step",
+    "ulysses_attention_step", "make_workspace", "StepGraph",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -391,3 +391,40 @@ def make_workspace(S, H, D, P, device, fused=True):
         w["qr"] = torch.empty((S, H, D), **e)
         w["kr"] = torch.empty((S, H, D), **e)
     return w
+
+
+class StepGraph:
+    """One ulysses_attention_step captured as a CUDA graph.
+
+    The step's kernels (norm/RoPE + seq2head of q and k, seq2head of v, one
+    attention launch per head group, head2seq) are captured once on the given
+    q, k, v, weights and positions; replay() re-runs all of them with a single
+    graph launch and none of the per-call host work (argument checks, tensor
+    map encoding, marshalling).  Inputs are read from the same buffers at
+    every replay: write new data into them (e.g. ``step.q.copy_(x)``) before
+    replaying.  Returns the same output tensor every time.
+    """
+
+    def __init__(self, q, k, v, w_q, w_k, pos, P, kv_len, d_t, d_h, d_w, eps=1e-6, theta=10000.0, fused=True):
+        S, H, D = q.shape
+        self.q, self.k, self.v, self.w_q, self.w_k, self.pos = q, k, v, w_q, w_k, pos
+        self.work = make_workspace(S, H, D, P, q.device, fused=fused)
+        args = (q, k, v, w_q, w_k, pos, P, kv_len, d_t, d_h, d_w, eps, theta)
+        side = torch.cuda.Stream(q.device)
+        side.wait_stream(torch.cuda.current_stream(q.device))
+        with torch.cuda.stream(side):
+            # one eager pass first: one-time library set-up (driver entry points,
+            # shared-memory attributes, the status word's address) stays out of the graph
+            ulysses_attention_step(*args, work=self.work, stream=side, fused=fused)
+        side.synchronize()
+        status = h3attn_get_device_status(side)
+        if status != H3ATTN_OK:
+            raise H3AttnError("StepGraph warm-up", status)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=side):
+            self.out = ulysses_attention_step(*args, work=self.work, stream=side, fused=fused)
+
+    def replay(self):
+        """Launch the captured step on the current stream; returns the output tensor."""
+        self.graph.replay()
+        return self.out

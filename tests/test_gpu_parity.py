@@ -231,6 +231,32 @@ def test_attention_argument_errors(h3, cuda_device):
     assert e.value.code == h3.H3ATTN_ERR_ALIAS
 
 
+def test_step_graph_replays_the_eager_step(h3, cuda_device):
+    """The whole step captured as a CUDA graph gives the eager step's output bit
+    for bit, also after new inputs are written into the captured buffers."""
+    w = synth.WORKLOADS["c2"]
+    dev = cuda_device
+    q, k, v = (t.to(dev) for t in synth.qkv(w))
+    wq, wk = (t.to(dev) for t in synth.norm_weights(w.D))
+    pos = torch.from_numpy(synth.packed_positions(w)).to(dev)
+    rest = (2, w.S_v, *w.rope_split, w.eps, w.theta)
+    eager = h3.ulysses_attention_step(q, k, v, wq, wk, pos, *rest).clone()
+    g = h3.StepGraph(q.clone(), k.clone(), v.clone(), wq, wk, pos, *rest)
+    out = g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    q2, k2, v2 = (synth.randn_bf16(tuple(q.shape), 700 + i, dev, zero_rows_from=w.S_v) for i in range(3))
+    g.q.copy_(q2)
+    g.k.copy_(k2)
+    g.v.copy_(v2)
+    out2 = g.replay().clone()
+    eager2 = h3.ulysses_attention_step(q2, k2, v2, wq, wk, pos, *rest)
+    torch.cuda.synchronize()
+    assert torch.equal(out2.view(torch.int16), eager2.view(torch.int16))
+    assert not torch.equal(out2.view(torch.int16), eager.view(torch.int16))
+    assert h3.h3attn_get_device_status() == 0
+
+
 def test_host_memory_is_refused_before_any_launch(h3, cuda_device):
     """Every call checks that its buffers are memory of the current device:
     host memory (pinned or pageable) is refused with H3ATTN_ERR_ARG and
