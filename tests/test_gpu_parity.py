@@ -139,6 +139,8 @@ def _attn(h3, dev, S, H, D, kv, seed=21, rows=None, heads=None):
     (300, 2, 64, 1),        # a single valid key
     (128, 2, 128, 128),     # second query tile entirely out of range
     (1000, 2, 128, 1000),   # eight key tiles, last partial
+    (1, 1, 64, 1),          # a one-token sequence: 255 of the block's 256 query rows past the end
+    (5, 3, 128, 3),         # five tokens, two of them padding
 ])
 def test_attention_matches_oracle(h3, cuda_device, S, H, D, kv):
     got, ref = _attn(h3, cuda_device, S, H, D, kv)
