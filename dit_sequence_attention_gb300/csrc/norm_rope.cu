@@ -13,10 +13,14 @@
 // is accurate to ~1e-16 even for positions in the thousands), then sincosf on
 // the reduced fp32 angle.  Each thread owns 8 consecutive dims (one 16-byte
 // vector) of a row, i.e. 4 whole rotation pairs; the D/8 threads of a row
-// reduce the sum of squares with warp shuffles.  Loads are issued four
+// reduce the sum of squares with warp shuffles.  A thread sits at the same
+// place in every row it handles, so it folds its 8 weights into its 4 pairs'
+// rotations once per token (out = inv * (f0 * w0 * (c, s) + f1 * w1 * (-s, c)),
+// three packed f32x2 operations per pair) and q and k are done one after the
+// other, each with its own folded coefficients.  Loads are issued four
 // vectors per thread at a time, the first batch before the angle work;
-// results leave with streaming (evict-first) stores.  Small blocks and few
-// registers keep many tokens in flight per SM.
+// results leave with streaming (evict-first) stores.  Small blocks (64
+// registers a thread) keep 8 tokens in flight per SM.
 // HBM-bound: 4 * H * D * 2 bytes per token (read and write q and k).
 //
 // With P > 1 the results are written straight into the Ulysses head-sharded
@@ -59,23 +63,25 @@ __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
     const int tok = blockIdx.x;  // b * S + s
     const int s = tok % S;
     const int cpt = H * VPR;      // vectors per tensor for this token
-    const int total = 2 * cpt;
-    const int iters = (total + kNormThreads - 1) / kNormThreads;
     const size_t tok_vec = static_cast<size_t>(tok) * cpt;
     const float inv_d = 1.0f / static_cast<float>(D);
 
-    // Issue the first batch of q/k loads before anything else, so their
-    // latency overlaps the position load and the angle computation below.
+    // This thread's position in a row, part = (vector index) % VPR, is the same
+    // for every vector it handles (the block size is a multiple of VPR and so is
+    // the tensor's vector count per token), so its 4 rotation pairs and 8
+    // weights are loaded once per token.
+    const int part = static_cast<int>(threadIdx.x) % VPR;
+
+    // Issue the first batch of q loads before anything else, so their latency
+    // overlaps the position load and the angle computation below.
+    const int iters = (cpt + kNormThreads - 1) / kNormThreads;  // per tensor
     uint4 x[kNormMaxVec];
 #pragma unroll
     for (int u = 0; u < kNormMaxVec; ++u) {
         const int idx = u * kNormThreads + threadIdx.x;
         x[u] = make_uint4(0, 0, 0, 0);
-        if (u < iters && idx < total) {
-            const bool is_k = idx >= cpt;
-            const size_t src = tok_vec + (is_k ? idx - cpt : idx);
-            if (in_bounds(st, src, 1, n_vec, kTagNormRope, 1)) x[u] = __ldcs((is_k ? k : q) + src);
-        }
+        if (u < iters && idx < cpt && in_bounds(st, tok_vec + idx, 1, n_vec, kTagNormRope, 1))
+            x[u] = __ldcs(q + tok_vec + idx);
     }
     if (threadIdx.x < D / 2) {
         const int pr = threadIdx.x;
@@ -89,74 +95,89 @@ __global__ void __launch_bounds__(kNormThreads) norm_rope_kernel(
         cs[pr] = make_float2(c, sn);
     }
     __syncthreads();
+    float2 rot[4];
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) rot[pp] = cs[part * 4 + pp];
 
-    for (int it0 = 0; it0 < iters; it0 += kNormMaxVec) {
-        if (it0 > 0) {
-#pragma unroll
-            for (int u = 0; u < kNormMaxVec; ++u) {
-                const int idx = (it0 + u) * kNormThreads + threadIdx.x;
-                x[u] = make_uint4(0, 0, 0, 0);
-                if (it0 + u < iters && idx < total) {
-                    const bool is_k = idx >= cpt;
-                    const size_t src = tok_vec + (is_k ? idx - cpt : idx);
-                    if (in_bounds(st, src, 1, n_vec, kTagNormRope, 3)) x[u] = __ldcs((is_k ? k : q) + src);
-                }
+#pragma unroll 1
+    for (int t = 0; t < 2; ++t) {  // q, then k
+        const uint4* src = t ? k : q;
+        uint4* out = t ? ko : qo;
+        // weight and rotation folded per pair (y0, y1) of this thread's 8 dims:
+        //   out0 = inv * (f0 * w0 c - f1 * w1 s),  out1 = inv * (f0 * w0 s + f1 * w1 c)
+        uint64_t ca[4], cb[4];
+        {
+            const float* w = (t ? wk : wq) + part * 8;
+            float wv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (in_bounds(st, static_cast<size_t>(part) * 8, 8, D, kTagNormRope, 4)) {
+                const float4 wa = __ldg(reinterpret_cast<const float4*>(w));
+                const float4 wb = __ldg(reinterpret_cast<const float4*>(w) + 1);
+                wv[0] = wa.x; wv[1] = wa.y; wv[2] = wa.z; wv[3] = wa.w;
+                wv[4] = wb.x; wv[5] = wb.y; wv[6] = wb.z; wv[7] = wb.w;
             }
-        }
-#pragma unroll
-        for (int u = 0; u < kNormMaxVec; ++u) {
-            if (it0 + u >= iters) break;  // uniform across the block
-            const int idx = (it0 + u) * kNormThreads + threadIdx.x;
-            const bool valid = idx < total;
-            const bool is_k = idx >= cpt;
-            const int c = is_k ? idx - cpt : idx;
-            const int part = c % VPR;
-            const uint32_t w4[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                f[2 * e] = bf16lo_to_f32(w4[e]);
-                f[2 * e + 1] = bf16hi_to_f32(w4[e]);
-            }
-            float ss = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-#pragma unroll
-            for (int off = VPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            if (!valid) continue;
-            const float inv = rsqrtf(ss * inv_d + eps);
-            if (!in_bounds(st, static_cast<size_t>(part) * 8, 8, D, kTagNormRope, 4)) continue;
-            const float4* wv = reinterpret_cast<const float4*>((is_k ? wk : wq) + part * 8);
-            const float4 wa = __ldg(wv), wb = __ldg(wv + 1);
-            const float wgt[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = f[e] * inv * wgt[e];
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp) {
-                const float2 r = cs[part * 4 + pp];
-                const float a = y[2 * pp], b = y[2 * pp + 1];
-                y[2 * pp] = a * r.x - b * r.y;
-                y[2 * pp + 1] = a * r.y + b * r.x;
+                const float w0 = wv[2 * pp], w1 = wv[2 * pp + 1], c = rot[pp].x, sn = rot[pp].y;
+                ca[pp] = f2_pack(w0 * c, w0 * sn);
+                cb[pp] = f2_pack(-(w1 * sn), w1 * c);
             }
-            uint4 out;
-            out.x = pack_bf16x2(y[0], y[1]);
-            out.y = pack_bf16x2(y[2], y[3]);
-            out.z = pack_bf16x2(y[4], y[5]);
-            out.w = pack_bf16x2(y[6], y[7]);
-            size_t dst = tok_vec + c;
-            if (kSharded) {  // head-sharded output: [g][s][j] with h = g * (H/P) + j
-                const int h = c / VPR;
-                // g = h / Hp by multiply and shift (hp_recip = ceil(2^32 / Hp); exact for h < 2^16)
-                const int g = static_cast<int>((static_cast<unsigned long long>(h) * hp_recip) >> 32);
-                dst = ((static_cast<size_t>(g) * S + s) * Hp + (h - g * Hp)) * VPR + part;
+        }
+        for (int it0 = 0; it0 < iters; it0 += kNormMaxVec) {
+            if (it0 > 0 || t > 0) {
+#pragma unroll
+                for (int u = 0; u < kNormMaxVec; ++u) {
+                    const int idx = (it0 + u) * kNormThreads + threadIdx.x;
+                    x[u] = make_uint4(0, 0, 0, 0);
+                    if (it0 + u < iters && idx < cpt && in_bounds(st, tok_vec + idx, 1, n_vec, kTagNormRope, 3))
+                        x[u] = __ldcs(src + tok_vec + idx);
+                }
             }
-            if (in_bounds(st, dst, 1, n_vec, kTagNormRope, 5)) __stcs((is_k ? ko : qo) + dst, out);
-            if (dbg != nullptr &&
-                in_bounds(st, (is_k ? dbg_k_offset : 0) + (tok_vec + c) * 8, 8, 2 * dbg_k_offset, kTagNormRope, 6)) {
-                float4* d4 = reinterpret_cast<float4*>(dbg + (is_k ? dbg_k_offset : 0) + (tok_vec + c) * 8);
-                d4[0] = make_float4(y[0], y[1], y[2], y[3]);
-                d4[1] = make_float4(y[4], y[5], y[6], y[7]);
+#pragma unroll
+            for (int u = 0; u < kNormMaxVec; ++u) {
+                if (it0 + u >= iters) break;  // uniform across the block
+                const int c = (it0 + u) * kNormThreads + threadIdx.x;  // vector index within the token's tensor
+                const uint32_t w4[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    f[2 * e] = bf16lo_to_f32(w4[e]);
+                    f[2 * e + 1] = bf16hi_to_f32(w4[e]);
+                }
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+#pragma unroll
+                for (int off = VPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (c >= cpt) continue;
+                const float inv = rsqrtf(ss * inv_d + eps);
+                const uint64_t inv2 = f2_pack(inv, inv);
+                float y[8];
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    const uint64_t r = f2_mul(f2_fma(f2_pack(f[2 * pp + 1], f[2 * pp + 1]), cb[pp],
+                                                     f2_mul(f2_pack(f[2 * pp], f[2 * pp]), ca[pp])),
+                                              inv2);
+                    f2_unpack(r, y[2 * pp], y[2 * pp + 1]);
+                }
+                uint4 o;
+                o.x = pack_bf16x2(y[0], y[1]);
+                o.y = pack_bf16x2(y[2], y[3]);
+                o.z = pack_bf16x2(y[4], y[5]);
+                o.w = pack_bf16x2(y[6], y[7]);
+                size_t dst = tok_vec + c;
+                if (kSharded) {  // head-sharded output: [g][s][j] with h = g * (H/P) + j
+                    const int h = c / VPR;
+                    // g = h / Hp by multiply and shift (hp_recip = ceil(2^32 / Hp); exact for h < 2^16)
+                    const int g = static_cast<int>((static_cast<unsigned long long>(h) * hp_recip) >> 32);
+                    dst = ((static_cast<size_t>(g) * S + s) * Hp + (h - g * Hp)) * VPR + part;
+                }
+                if (in_bounds(st, dst, 1, n_vec, kTagNormRope, 5)) __stcs(out + dst, o);
+                if (dbg != nullptr &&
+                    in_bounds(st, (t ? dbg_k_offset : 0) + (tok_vec + c) * 8, 8, 2 * dbg_k_offset, kTagNormRope, 6)) {
+                    float4* d4 = reinterpret_cast<float4*>(dbg + (t ? dbg_k_offset : 0) + (tok_vec + c) * 8);
+                    d4[0] = make_float4(y[0], y[1], y[2], y[3]);
+                    d4[1] = make_float4(y[4], y[5], y[6], y[7]);
+                }
             }
         }
     }
