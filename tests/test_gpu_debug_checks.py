@@ -73,7 +73,8 @@ def test_norm_rope(h3, cuda_device, D, split, P):
     S, H = 301 if P == 1 else 300, 8
     q, k = synth.randn_bf16((S, H, D), 21, cuda_device), synth.randn_bf16((S, H, D), 22, cuda_device)
     wq, wk = (t.to(cuda_device) for t in synth.norm_weights(D))
-    pos = torch.randint(0, 50, (S, 3), dtype=torch.int32, device=cuda_device)
+    pos = torch.randint(0, 50, (S, 3), dtype=torch.int32,
+                        generator=torch.Generator().manual_seed(61)).to(cuda_device)
 
     def run():
         dbg32 = torch.empty((2, S, H, D), dtype=torch.float32, device=cuda_device)

@@ -57,7 +57,8 @@ def test_norm_rope_stays_in_bounds(h3, cuda_device, S, D):
     split = (16, 24, 24) if D == 64 else (32, 48, 48)
     q, k = synth.randn_bf16((S, H, D), 1, cuda_device), synth.randn_bf16((S, H, D), 2, cuda_device)
     wq, wk = (t.to(cuda_device) for t in synth.norm_weights(D))
-    pos = torch.randint(0, 50, (S, 3), dtype=torch.int32, device=cuda_device)
+    pos = torch.randint(0, 50, (S, 3), dtype=torch.int32,
+                        generator=torch.Generator().manual_seed(62)).to(cuda_device)
     rq, qo = guarded((S, H, D), cuda_device)
     rk, ko = guarded((S, H, D), cuda_device)
     h3.h3attn_qk_norm_rope(q, k, qo, ko, wq, wk, pos, *split)
@@ -91,7 +92,8 @@ def test_fused_norm_rope_seq2head_stays_in_bounds(h3, cuda_device):
     S, H, D, P = 202, 8, 128, 2
     q, k = synth.randn_bf16((S, H, D), 3, cuda_device), synth.randn_bf16((S, H, D), 4, cuda_device)
     wq, wk = (t.to(cuda_device) for t in synth.norm_weights(D))
-    pos = torch.randint(0, 50, (S, 3), dtype=torch.int32, device=cuda_device)
+    pos = torch.randint(0, 50, (S, 3), dtype=torch.int32,
+                        generator=torch.Generator().manual_seed(63)).to(cuda_device)
     rq, qh = guarded((P, S, H // P, D), cuda_device)
     rk, kh = guarded((P, S, H // P, D), cuda_device)
     h3.h3attn_qk_norm_rope_seq2head(q, k, qh, kh, wq, wk, pos, P, 32, 48, 48)
