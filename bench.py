@@ -57,7 +57,10 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-proj", action="store_true", help="skip timing the all-gather variant's fp8 projection")
-    ap.add_argument("--no-graph", action="store_true", help="skip timing the step replayed as a CUDA graph")
+    ap.add_argument("--graph", action="store_true", help="also time the step replayed as a CUDA graph (StepGraph)")
+    ap.add_argument("--long-steps", type=int, default=3,
+                    help="timed steps of the 1080p leg that follows a shorter headline workload (0: skip it)")
+    ap.add_argument("--long-warmup", type=int, default=2)
     ap.add_argument("--no-chunks", action="store_true",
                     help="skip timing the step with head-chunked attention and overlapped output exchange")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -99,18 +102,40 @@ def load_peaks(path=None):
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+ATTN_SOURCES = [os.path.join(ROOT, "dit_sequence_attention_gb300", "csrc", f)
+                for f in ("attention.cu", "h3_device.cuh")]
+
+
+def attention_fingerprint():
+    """sha256 (first 16 hex digits) of the attention kernel's sources."""
+    import hashlib
+    h = hashlib.sha256()
+    for path in ATTN_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def read_traffic():
-    """Per-launch DRAM bytes of the attention kernel from the committed ncu summary, if any."""
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, or None when that capture was taken on other kernel sources
+    (the summary records the fingerprint of the sources it measured)."""
     if not os.path.exists(TRAFFIC_FILE):
-        return None
+        return None, None
+    vals = {}
     with open(TRAFFIC_FILE) as f:
         for line in f:
-            if line.startswith("traffic_bytes_per_launch_480p_group28:"):
-                try:
-                    return float(line.split(":", 1)[1].split()[0])
-                except ValueError:
-                    return None
-    return None
+            if ":" in line and not line.startswith(" "):
+                key, val = line.split(":", 1)
+                vals[key.strip()] = val.strip().split()[0] if val.strip() else ""
+    fp = vals.get("attention_sources_sha256_16")
+    try:
+        traffic = float(vals["traffic_bytes_per_launch_480p_group28"])
+    except (KeyError, ValueError):
+        return None, None
+    if fp != attention_fingerprint():
+        return None, "committed capture is of other attention sources"
+    return traffic, "profiles/attention_dram_traffic.txt (committed ncu capture of the same kernel sources)"
 
 
 class ClockSampler:
@@ -275,13 +300,133 @@ def workload_config(w, P):
             "ulysses_P": P, "l2": f"inputs larger than L2 ({w.S * w.H * w.D * 2 / 1e6:.0f} MB per tensor); no flush"}
 
 
+class StepRunner:
+    """The bench step on one workload's buffers: fused QK-norm+RoPE+seq2head of
+    q and k, seq2head of v, one attention launch per head group, head2seq.
+    Records CUDA events around each launch on the launching stream."""
+
+    def __init__(self, h3, w, P, q, k, v, wq, wk, pos, stream):
+        self.h3, self.w, self.P = h3, w, P
+        self.q, self.k, self.v, self.wq, self.wk, self.pos = q, k, v, wq, wk, pos
+        self.stream = stream
+        self.work = h3.make_workspace(w.S, w.H, w.D, P, q.device)
+        self.ev = {"norm": [], "s2h": [], "attn": [], "h2s": []}
+
+    def _mark(self):
+        import torch
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(self.stream)
+        return e
+
+    def step(self, record=False):
+        h3, w, P, work = self.h3, self.w, self.P, self.work
+        mark = self._mark if record else (lambda: None)
+        e0 = mark()
+        h3.h3attn_qk_norm_rope_seq2head(self.q, self.k, work["qh"], work["kh"], self.wq, self.wk, self.pos, P,
+                                        *w.rope_split, w.eps, w.theta, stream=self.stream)
+        e1 = mark()
+        h3.h3attn_seq2head(self.v, work["vh"], P, self.stream)
+        e2 = mark()
+        marks = []
+        for g in range(P):
+            h3.h3attn_forward(work["qh"][g], work["kh"][g], work["vh"][g], work["oh"][g], kv_len=w.S_v,
+                              stream=self.stream)
+            marks.append(mark())
+        h3.h3attn_head2seq(work["oh"], work["o"], P, self.stream)
+        e4 = mark()
+        if record:
+            self.ev["norm"].append((e0, e1))
+            self.ev["s2h"].append((e1, e2))
+            prev = e2
+            for m in marks:
+                self.ev["attn"].append((prev, m))
+                prev = m
+            self.ev["h2s"].append((marks[-1], e4))
+
+    def avg_ms(self, name):
+        xs = [a.elapsed_time(b) for a, b in self.ev[name]]
+        return sum(xs) / len(xs)
+
+    def launches_per_step(self):
+        return 1 + 1 + self.P + 1
+
+
+def timed_region(runner, steps, warmup, world, dev, local, barrier):
+    """W untimed steps, then exactly `steps` steps between CUDA events on the
+    launching stream, bracketed by a barrier and a device synchronisation on
+    both sides, with nvidia-smi clock sampling during the timed steps.
+    Returns (max-over-ranks elapsed ms, clock summary)."""
+    import torch
+    h3 = runner.h3
+    for _ in range(warmup):
+        runner.step()
+    torch.cuda.synchronize(dev)
+    if h3.h3attn_get_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(runner.stream)
+    for _ in range(steps):
+        runner.step(record=True)
+    t_end.record(runner.stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    status = h3.h3attn_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    return max_over_ranks(t_start.elapsed_time(t_end), world, dev), clk
+
+
+def attention_roofline(w, P, attn_ms, peaks, peak_src, clk, n_sm):
+    """Roofline of one attention launch (one head group): algorithmic flops
+    4 * S_v^2 * D * (H / P) over its CUDA-event duration, against the measured
+    dense bf16 burst peak (the sustained figure beside it)."""
+    flops_launch = w.attention_flops(heads=w.H // P)
+    achieved = flops_launch / (attn_ms * 1e-3) / 1e12
+    clock_peak = (n_sm * BF16_FLOP_PER_CLK_SM * clk["sm_mhz"] * 1e6 / 1e12) if clk else None
+    return {"kernel": f"attn_fwd_kernel<{w.D}> (one {w.H // P}-head group launch)",
+            "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"],
+            "peak_source": f"{peak_src} bf16 dense, burst",
+            "sustained_peak": peaks["bf16_tflops_sustained"],
+            "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+            "algorithmic_flops_per_launch": flops_launch, "ms_per_launch": attn_ms,
+            "tensor_peak_at_median_clock": clock_peak,
+            "frac_of_tensor_peak_at_median_clock": (achieved / clock_peak) if clock_peak else None}
+
+
+def hbm_kernels(runner, peaks):
+    w = runner.w
+    tensor_bytes = w.S * w.H * w.D * 2
+    ks = {"qk_norm_rope_seq2head": ("norm", 4), "seq2head_v": ("s2h", 2), "head2seq": ("h2s", 2)}
+    out = {}
+    for name, (ev, mult) in ks.items():
+        ms = runner.avg_ms(ev)
+        gbs = mult * tensor_bytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "GB_per_s": gbs, "algorithmic_bytes": mult * tensor_bytes,
+                     "frac_of_hbm_peak": gbs / peaks["hbm_gbs"], "frac_of_hbm_spec": gbs / HBM_SPEC_GBS}
+    return out
+
+
+def make_inputs(w, dev, rank):
+    """Seeded N(0,1) q, k, v of this rank's own sequence (pad rows zero)."""
+    from dit_sequence_attention_gb300 import synth
+    return tuple(synth.randn_bf16((w.S, w.H, w.D), seed + 1000 * rank, dev, zero_rows_from=w.S_v)
+                 for seed in (synth.SEED_Q, synth.SEED_K, synth.SEED_V))
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
-    import numpy as np
     import torch
     import dit_sequence_attention_gb300 as h3
     from dit_sequence_attention_gb300 import synth
@@ -293,98 +438,33 @@ def main():
     P = args.P
     S, H, D = w.S, w.H, w.D
     # each rank draws its own sequence (independent problems, weak scaling)
-    q, k, v = (synth.randn_bf16((S, H, D), seed + 1000 * rank, dev, zero_rows_from=w.S_v)
-               for seed in (synth.SEED_Q, synth.SEED_K, synth.SEED_V))
+    q, k, v = make_inputs(w, dev, rank)
     wq, wk = (t.to(dev) for t in synth.norm_weights(D))
     pos = torch.from_numpy(synth.packed_positions(w)).to(dev)
-    work = h3.make_workspace(S, H, D, P, dev)
     stream = torch.cuda.current_stream(dev)
-
-    ev = {"norm": [], "s2h": [], "attn": [], "h2s": []}   # norm = fused norm/RoPE + seq2head of q, k
-
-    def step(record=False):
-        def mark():
-            e = torch.cuda.Event(enable_timing=True)
-            e.record(stream)
-            return e
-        e0 = mark() if record else None
-        h3.h3attn_qk_norm_rope_seq2head(q, k, work["qh"], work["kh"], wq, wk, pos, P, *w.rope_split, w.eps,
-                                        w.theta)
-        e1 = mark() if record else None
-        h3.h3attn_seq2head(v, work["vh"], P)
-        e2 = mark() if record else None
-        marks = []
-        for g in range(P):
-            h3.h3attn_forward(work["qh"][g], work["kh"][g], work["vh"][g], work["oh"][g], kv_len=w.S_v)
-            if record:
-                marks.append(mark())
-        h3.h3attn_head2seq(work["oh"], work["o"], P)
-        e4 = mark() if record else None
-        if record:
-            ev["norm"].append((e0, e1))
-            ev["s2h"].append((e1, e2))
-            prev = e2
-            for m in marks:
-                ev["attn"].append((prev, m))
-                prev = m
-            ev["h2s"].append((marks[-1], e4))
+    runner = StepRunner(h3, w, P, q, k, v, wq, wk, pos, stream)
+    work = runner.work
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    if h3.h3attn_get_device_status() != 0:
-        raise RuntimeError("device status error during warm-up")
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    barrier()
-    torch.cuda.synchronize(dev)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for _ in range(args.steps):
-        step(record=True)
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    clk = clocks.stop()
-    status = h3.h3attn_get_device_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed region")
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-
-    def avg(name):
-        xs = [a.elapsed_time(b) for a, b in ev[name]]
-        return sum(xs) / len(xs)
-
+    elapsed_ms, clk = timed_region(runner, args.steps, args.warmup, world, dev, local, barrier)
     flops_seq = w.attention_flops()
     value = job_tflops(flops_seq, args.steps, world, elapsed_ms)
     ms_step = elapsed_ms / args.steps
-    attn_ms = avg("attn")                                   # per launch (one head group)
-    flops_launch = w.attention_flops(heads=H // P)
-    achieved = flops_launch / (attn_ms * 1e-3) / 1e12
+    attn_ms = runner.avg_ms("attn")                         # per launch (one head group)
     peaks, peak_src = load_peaks()
-    peak = peaks["bf16_tflops_sustained"]
-    traffic = read_traffic() if (P == 2 and w.name == "480p" and D == 128) else None
-    tensor_bytes = S * H * D * 2
-    kernels = {
-        "qk_norm_rope_seq2head": {"ms": avg("norm"), "GB_per_s": 4 * tensor_bytes / (avg("norm") * 1e-3) / 1e9},
-        "seq2head_v": {"ms": avg("s2h"), "GB_per_s": 2 * tensor_bytes / (avg("s2h") * 1e-3) / 1e9},
-        "attention_per_group": {"ms": attn_ms, "TFLOP_per_s": achieved},
-        "head2seq": {"ms": avg("h2s"), "GB_per_s": 2 * tensor_bytes / (avg("h2s") * 1e-3) / 1e9},
-    }
-    hbm_peak = peaks["hbm_gbs"]
-    for kname in ("qk_norm_rope_seq2head", "seq2head_v", "head2seq"):
-        kernels[kname]["frac_of_hbm_peak"] = kernels[kname]["GB_per_s"] / hbm_peak
-        kernels[kname]["frac_of_hbm_spec"] = kernels[kname]["GB_per_s"] / HBM_SPEC_GBS
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    clock_peak = (n_sm * BF16_FLOP_PER_CLK_SM * clk["sm_mhz"] * 1e6 / 1e12) if clk else None
+    roofline = attention_roofline(w, P, attn_ms, peaks, peak_src, clk, n_sm)
+    traffic, traffic_src = read_traffic() if (P == 2 and w.name == "480p" and D == 128) else (None, None)
+    roofline["traffic"] = traffic
+    roofline["traffic_source"] = traffic_src
+    roofline["attention_sources_sha256_16"] = attention_fingerprint()
+    kernels = hbm_kernels(runner, peaks)
+    kernels["attention_per_group"] = {"ms": attn_ms, "TFLOP_per_s": roofline["achieved"]}
+    tensor_bytes = S * H * D * 2
 
     # ---------------------------------------------------------------- e2e
     # Through the public API from pinned host buffers: every step copies its
@@ -445,6 +525,29 @@ def main():
     e2e_value = job_tflops(flops_seq, e2e_steps, world, e2e_ms)
     h2d = 3 * tensor_bytes + hpos.numel() * 4
     d2h = tensor_bytes
+    del hq, hk, hv, hout, dins, works
+
+    # --------------------------------------- the 262k end of the metric: 1080p
+    # A short leg on the 1080p-like sequence (262,144 tokens) with the same
+    # step and launch configuration, timed the same way; the headline above
+    # stays on the bench workload.
+    long_leg = None
+    if args.long_steps > 0 and w.name != "1080p" and D == 128:
+        wl = synth.WORKLOADS["1080p"]
+        ql, kl, vl = make_inputs(wl, dev, rank)
+        posl = torch.from_numpy(synth.packed_positions(wl)).to(dev)
+        rl = StepRunner(h3, wl, P, ql, kl, vl, wq, wk, posl, stream)
+        el_ms, clk_l = timed_region(rl, args.long_steps, args.long_warmup, world, dev, local, barrier)
+        ms_l = el_ms / args.long_steps
+        long_leg = {
+            "1080p": {"config": workload_config(wl, P), "steps": args.long_steps, "warmup": args.long_warmup,
+                      "ms_per_step": ms_l, "value": job_tflops(wl.attention_flops(), args.long_steps, world, el_ms),
+                      "unit": "TFLOP/s",
+                      "tokens_per_s": wl.S_v * args.long_steps * world / (el_ms * 1e-3),
+                      "roofline": attention_roofline(wl, P, rl.avg_ms("attn"), peaks, peak_src, clk_l, n_sm),
+                      "kernels": hbm_kernels(rl, peaks), "clocks": clk_l,
+                      "gpu_launches": args.long_steps * rl.launches_per_step()}}
+        del ql, kl, vl, rl
 
     # ------------------------------- head-chunked attention, overlapped exchange
     # The same step with each group's heads split into chunks; the output
@@ -482,49 +585,33 @@ def main():
         del ref_out
 
     # ------------------------------------------------ whole step as a CUDA graph
-    # One graph launch per step instead of five library calls: no per-call host
-    # work.  Timed at the bench workload and at c2 (4,096 tokens), where the
-    # host side of eager calls is a visible share of the step.
     graph_runs = None
-    if not args.no_graph and D == 128:
-        graph_runs = {}
-        for wname in dict.fromkeys((w.name, "c2")):
-            ww = synth.WORKLOADS[wname]
-            if wname == w.name:
-                gq, gk, gv, gpos = q, k, v, pos
-            else:
-                gq, gk, gv = (synth.randn_bf16((ww.S, ww.H, ww.D), 500 + i, dev, zero_rows_from=ww.S_v)
-                              for i in range(3))
-                gpos = torch.from_numpy(synth.packed_positions(ww)).to(dev)
-            gargs = (P, ww.S_v, *ww.rope_split, ww.eps, ww.theta)
-            sg = h3.StepGraph(gq, gk, gv, wq, wk, gpos, *gargs)
-            gwork = h3.make_workspace(ww.S, ww.H, ww.D, P, dev)
-            n_g = max(3, min(args.steps, 20)) if wname == w.name else 200
+    if args.graph and D == 128:
+        sg = h3.StepGraph(q, k, v, wq, wk, pos, P, w.S_v, *w.rope_split, w.eps, w.theta)
+        gwork = h3.make_workspace(S, H, D, P, dev)
+        n_g = max(3, min(args.steps, 20))
 
-            def timed(fn, n):
-                for _ in range(3):
-                    fn()
-                torch.cuda.synchronize(dev)
-                ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                ga.record(stream)
-                for _ in range(n):
-                    fn()
-                gb.record(stream)
-                torch.cuda.synchronize(dev)
-                return ga.elapsed_time(gb) / n
+        def timed(fn, n):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize(dev)
+            ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ga.record(stream)
+            for _ in range(n):
+                fn()
+            gb.record(stream)
+            torch.cuda.synchronize(dev)
+            return ga.elapsed_time(gb) / n
 
-            eager_ms = timed(lambda: h3.ulysses_attention_step(gq, gk, gv, wq, wk, gpos, *gargs, work=gwork,
-                                                               stream=stream), n_g)
-            graph_ms = timed(sg.replay, n_g)
-            if h3.h3attn_get_device_status() != 0:
-                raise RuntimeError("device status error in the graph timing")
-            if not torch.equal(sg.out.view(torch.int16), gwork["o"].view(torch.int16)):
-                raise RuntimeError(f"graph replay differs from the eager step ({wname})")
-            graph_runs[wname] = {"tokens": ww.S, "eager_ms_per_step": eager_ms, "graph_ms_per_step": graph_ms,
-                                 "steps": n_g}
-            del sg, gwork
-        graph_runs["note"] = ("StepGraph: the whole step captured once, replayed with one graph launch; "
-                              "outputs checked bit-identical to the eager step")
+        eager_ms = timed(lambda: h3.ulysses_attention_step(q, k, v, wq, wk, pos, P, w.S_v, *w.rope_split, w.eps,
+                                                           w.theta, work=gwork, stream=stream), n_g)
+        graph_ms = timed(sg.replay, n_g)
+        if h3.h3attn_get_device_status() != 0:
+            raise RuntimeError("device status error in the graph timing")
+        if not torch.equal(sg.out.view(torch.int16), gwork["o"].view(torch.int16)):
+            raise RuntimeError("graph replay differs from the eager step")
+        graph_runs = {"eager_ms_per_step": eager_ms, "graph_ms_per_step": graph_ms, "steps": n_g}
+        del sg, gwork
 
     # ---------------------------------------------- all-gather variant projection
     proj = None
@@ -569,25 +656,19 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v, random-init norm weights)",
         "config": workload_config(w, P),
         "tokens_per_s": w.S_v * args.steps * world / (elapsed_ms * 1e-3),
-        "frac_of_bf16_peak": value / peak,
+        "frac_of_bf16_peak": value / peaks["bf16_tflops"],
         "padded_work_tflops": value * S / w.S_v,
         "padded_work_note": "the same step counted as 4*S*S_v*D*H (every padded query row against the valid keys)",
-        "roofline": {"kernel": "attn_fwd_kernel<128> (one 28-head group launch)" if D == 128 else "attn_fwd_kernel",
-                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16 dense, sustained",
-                     "burst_peak": peaks["bf16_tflops"], "frac_of_burst": achieved / peaks["bf16_tflops"],
-                     "algorithmic_flops_per_launch": flops_launch,
-                     "tensor_peak_at_median_clock": clock_peak,
-                     "frac_of_tensor_peak_at_median_clock": (achieved / clock_peak) if clock_peak else None},
+        "roofline": roofline,
         "kernels": kernels,
-        "hbm_peak_GB_per_s": hbm_peak,
+        "hbm_peak_GB_per_s": peaks["hbm_gbs"],
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
                 "note": "pinned host q/k/v/pos -> device, whole path, device -> pinned host output each step; "
                         "copies double-buffered on a second stream, overlapping compute"},
-        "gpu_launches": args.steps * (1 + 1 + P + 1),
+        "gpu_launches": args.steps * runner.launches_per_step(),
         "clocks": clk,
+        "workloads": long_leg,
         "cpu_baseline": cpu,
         "ag_qkv_proj_fp8": proj,
         "head_chunk_overlap": chunk_runs,

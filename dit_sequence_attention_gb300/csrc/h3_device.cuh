@@ -16,17 +16,26 @@ namespace h3 {
 // ----------------------------------------------------------------------------
 // Device-side status word.  A kernel that gives up on a wait records
 // H3ATTN_ERR_DEVICE_TIMEOUT here (first error wins) and returns normally; the
-// host reads and clears it through h3attn_get_device_status().  Kernels get
-// its address as an argument (one word per device, owned by the library).
+// host takes it (reads and clears it in one atomic exchange) through
+// h3attn_get_device_status().  Kernels get its address as an argument (one
+// word per device, owned by the library).  Code and diagnostic info share one
+// 64-bit word, so an error is recorded and taken whole or not at all:
+//   bits 56-63  -code (1..255; 0 = no error)   bits 0-55  info
 // ----------------------------------------------------------------------------
 struct DeviceStatus {
-    int code;
-    int pad;
-    unsigned long long info;
+    unsigned long long word;
 };
 
+__host__ __device__ constexpr unsigned long long status_pack(int code, unsigned long long info) {
+    return (static_cast<unsigned long long>(-code & 0xff) << 56) | (info & 0x00ffffffffffffffull);
+}
+__host__ __device__ constexpr int status_code(unsigned long long word) { return -static_cast<int>(word >> 56); }
+__host__ __device__ constexpr unsigned long long status_info(unsigned long long word) {
+    return word & 0x00ffffffffffffffull;
+}
+
 __device__ __forceinline__ void record_device_error(DeviceStatus* st, int code, unsigned long long info) {
-    if (atomicCAS(&st->code, 0, code) == 0) st->info = info;
+    atomicCAS(&st->word, 0ull, status_pack(code, info));
 }
 
 // Kernel tags of the status info word.

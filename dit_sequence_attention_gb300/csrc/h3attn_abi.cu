@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cmath>
+#include <atomic>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
@@ -18,11 +19,15 @@
 
 namespace h3 {
 
-__device__ DeviceStatus g_status;
+constexpr int kMaxDevices = 64;
 
-int device_status_ptr(DeviceStatus** out) {
-    constexpr int kMaxDevices = 64;
+// One status word per device, and the slot the take kernel copies it into.
+__device__ DeviceStatus g_status;
+__device__ unsigned long long g_status_taken;
+
+static int status_ptrs(DeviceStatus** status, unsigned long long** taken) {
     static DeviceStatus* cache[kMaxDevices] = {};
+    static unsigned long long* cache_taken[kMaxDevices] = {};
     static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -31,11 +36,24 @@ int device_status_ptr(DeviceStatus** out) {
     std::lock_guard<std::mutex> lock(mu);
     if (cache[dev] == nullptr) {
         void* p = nullptr;
+        void* t = nullptr;
         if ((e = cudaGetSymbolAddress(&p, g_status)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaGetSymbolAddress(&t, g_status_taken)) != cudaSuccess) return cuda_fail(e);
         cache[dev] = static_cast<DeviceStatus*>(p);
+        cache_taken[dev] = static_cast<unsigned long long*>(t);
     }
-    *out = cache[dev];
+    *status = cache[dev];
+    if (taken != nullptr) *taken = cache_taken[dev];
     return H3ATTN_OK;
+}
+
+int device_status_ptr(DeviceStatus** out) { return status_ptrs(out, nullptr); }
+
+// Read and clear the status word in one atomic exchange, so an error that a
+// kernel on another stream records at the same moment is either taken whole
+// now or left for the next read -- never erased unseen.
+__global__ void status_take_kernel(DeviceStatus* st, unsigned long long* taken) {
+    *taken = atomicExch(&st->word, 0ull);
 }
 
 int ensure_smem_attr(const void* kernel, int bytes) {
@@ -62,7 +80,8 @@ int ensure_smem_attr(const void* kernel, int bytes) {
 }
 
 static thread_local int t_last_cuda_error = 0;
-static unsigned long long g_last_info = 0;
+// Diagnostic info of the last device error taken on each device.
+static std::atomic<unsigned long long> g_last_info[kMaxDevices];
 
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -131,6 +150,11 @@ int launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream) {
 // ----------------------------------------------------------------------------
 // Host-side checks
 // ----------------------------------------------------------------------------
+// The norm kernel finds a head's group by multiplying with ceil(2^32 / (H/P))
+// and shifting; that is exact while (H - 1) * (H/P) < 2^32, which every H up
+// to 65535 satisfies.
+constexpr int kMaxNormHeads = 65535;
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 static bool overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -196,7 +220,14 @@ int h3attn_build_flags(void) { return H3ATTN_DEBUG_CHECKS ? H3ATTN_BUILD_DEBUG_C
 
 int h3attn_last_cuda_error(void) { return t_last_cuda_error; }
 
-unsigned long long h3attn_last_device_error_info(void) { return g_last_info; }
+unsigned long long h3attn_last_device_error_info(void) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return g_last_info[dev].load();
+}
 
 const char* h3attn_strerror(int code) {
     switch (code) {
@@ -221,7 +252,7 @@ int h3attn_qk_norm_rope(const void* q, const void* k, void* q_out, void* k_out, 
         !aligned16(w_k) || (dbg_fp32 && !aligned16(dbg_fp32)))
         return H3ATTN_ERR_ARG;
     if (!(eps >= 0.0f) || !(theta > 0.0f)) return H3ATTN_ERR_ARG;
-    if (B < 1 || S < 1 || H < 1 || (D != 64 && D != 128)) return H3ATTN_ERR_SHAPE;
+    if (B < 1 || S < 1 || H < 1 || H > kMaxNormHeads || (D != 64 && D != 128)) return H3ATTN_ERR_SHAPE;
     if (d_t < 0 || d_h < 0 || d_w < 0 || (d_t | d_h | d_w) & 1 || d_t + d_h + d_w != D) return H3ATTN_ERR_SHAPE;
     if (static_cast<uint64_t>(B) * S >= (1ull << 31)) return H3ATTN_ERR_SHAPE;
     const size_t bytes = static_cast<size_t>(B) * S * H * D * 2;
@@ -246,9 +277,10 @@ int h3attn_qk_norm_rope_seq2head(const void* q, const void* k, void* qh_out, voi
         !aligned16(w_k) || (dbg_fp32 && !aligned16(dbg_fp32)))
         return H3ATTN_ERR_ARG;
     if (!(eps >= 0.0f) || !(theta > 0.0f)) return H3ATTN_ERR_ARG;
-    if (S < 1 || H < 1 || P < 1 || (D != 64 && D != 128)) return H3ATTN_ERR_SHAPE;
+    if (S < 1 || H < 1 || H > kMaxNormHeads || P < 1 || (D != 64 && D != 128)) return H3ATTN_ERR_SHAPE;
     if (S % P != 0 || H % P != 0) return H3ATTN_ERR_SHAPE;
     if (d_t < 0 || d_h < 0 || d_w < 0 || (d_t | d_h | d_w) & 1 || d_t + d_h + d_w != D) return H3ATTN_ERR_SHAPE;
+    if (static_cast<uint64_t>(S) * H * D / 8 >= (1ull << 32)) return H3ATTN_ERR_SHAPE;
     const size_t bytes = static_cast<size_t>(S) * H * D * 2;
     // the output is a permutation of the input, so it may not share memory with it
     if (overlap(q, bytes, qh_out, bytes) || overlap(k, bytes, kh_out, bytes) || overlap(q, bytes, kh_out, bytes) ||
@@ -271,9 +303,20 @@ int h3attn_forward(const void* q, const void* k, const void* v, void* o, int B, 
     if (B < 1 || S < 1 || H_buf < 1 || (D != 64 && D != 128)) return H3ATTN_ERR_SHAPE;
     if (head_begin < 0 || head_count < 1 || head_begin + head_count > H_buf || head_count > 65535)
         return H3ATTN_ERR_SHAPE;
-    if (kv_len != nullptr)
+    if (kv_len != nullptr) {
+        // kv_len is read here, on the host: refuse device memory before touching it.
+        // Host memory (pageable or pinned) reports success with a host type; if
+        // the query itself fails there is no usable CUDA device, so the pointer
+        // cannot be device memory (the device check below then fails the call).
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, kv_len) == cudaSuccess) {
+            if (a.type == cudaMemoryTypeDevice) return H3ATTN_ERR_ARG;
+        } else {
+            (void)cudaGetLastError();
+        }
         for (int b = 0; b < B; ++b)
             if (kv_len[b] < 1 || kv_len[b] > S) return H3ATTN_ERR_SHAPE;
+    }
     const size_t item = static_cast<size_t>(S) * H_buf * D * 2;
     const size_t bytes = item * B;
     if (overlap(o, bytes, q, bytes) || overlap(o, bytes, k, bytes) || overlap(o, bytes, v, bytes))
@@ -351,20 +394,26 @@ int h3attn_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, 
 }
 
 int h3attn_get_device_status(void* stream) {
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e);
-    DeviceStatus* dst = nullptr;
-    int rc = device_status_ptr(&dst);
+    static std::mutex mu[kMaxDevices];  // one take in flight per device: the copy-out slot is shared
+    DeviceStatus* st = nullptr;
+    unsigned long long* taken = nullptr;
+    int rc = status_ptrs(&st, &taken);
     if (rc != H3ATTN_OK) return rc;
-    DeviceStatus st{};
-    if ((e = cudaMemcpy(&st, dst, sizeof(st), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
-    if (st.code != 0) {
-        g_last_info = st.info;
-        const DeviceStatus zero{};
-        if ((e = cudaMemcpy(dst, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess) return cuda_fail(e);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned long long word = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu[dev]);
+        status_take_kernel<<<1, 1, 0, s>>>(st, taken);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaMemcpyAsync(&word, taken, sizeof(word), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
     }
-    const int status = st.code;
-    return status;
+    if (word != 0) g_last_info[dev].store(status_info(word));
+    return status_code(word);
 }
 
 int h3attn_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {

@@ -9,25 +9,21 @@
 // for part in (q, k, v) and c < inner/P, written as bf16 [S][inner/P] per part
 // (the head-sharded [S][H/P][D] layout the attention kernel reads).
 //
-// Persistent clusters of two CTAs (one CTA per SM).  A cluster walks pairs of
-// output tiles that share their 256 weight rows: CTA rank r takes tokens
-// [256*p + 128*r, +128).  Each CTA loads its own x slice and HALF of the
-// weight slice, multicast into both CTAs' shared memory, so every weight byte
-// crosses L2 once per pair instead of once per tile.  192 threads per CTA:
+// Persistent: one CTA per SM walks output tiles of 128 tokens x 256 output
+// features of one part (tile t, t + grid, ...), 192 threads:
 //   warp 0      TMA producer: x and w slices of 128 bytes along K into a
-//               4-stage ring (128B swizzle) that runs across tiles; a stage
-//               is refilled only after the MMAs of BOTH CTAs released it.
+//               4-stage ring (128B swizzle) that runs across tiles.
 //   warp 1      allocates 512 TMEM columns = two 128x256 fp32 accumulators;
 //               one lane issues 4 MMAs (K = 32) per stage with descriptors
 //               built once (start-address offsets only).
 //   warps 2-5   epilogue: TMEM -> registers, times scale, bf16, global stores;
 //               while they drain one accumulator the MMAs fill the other.
-// Tile pairs are numbered with the output-feature tile fastest, so clusters
-// that run at the same time share their x rows through L2; the weight slice
-// (58 MB at P = 2) stays L2-resident.  A cluster barrier at the end keeps a
-// CTA alive until its partner can no longer write into it.  Each output element's K accumulation order is the same
-// whatever the rank or tile, so the per-rank projections are bit-identical to
-// the matching columns of the full (P = 1) projection.
+// Every CTA loads its own operands, with plain TMA copies into its own shared memory.
+// Tiles are numbered with the output-feature tile fastest, so the CTAs that
+// run at the same time share their x rows through L2; the weight slice
+// (58 MB at P = 2) stays L2-resident.  Each output element's K accumulation
+// order is the same whatever the rank or tile, so the per-rank projections are
+// bit-identical to the matching columns of the full (P = 1) projection.
 #include <cuda.h>
 
 #include "h3_device.cuh"
@@ -66,7 +62,7 @@ struct ProjParams {
     int n_kblocks;
     int tiles_per_part;
     int n_tiles_n;          // 3 * tiles_per_part
-    int n_pairs;            // n_tiles_n * ceil(token tiles / 2)
+    int n_tiles;            // n_tiles_n * token tiles
     float scale;
     unsigned long long wait_limit_ns;
     DeviceStatus* status;
@@ -89,34 +85,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const void* tmap,
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t smem_dst, const void* tmap, uint32_t bar, int c0, int c1,
-                                               uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
-
-// Arrive on `bar` in every CTA of `cta_mask` once this thread's MMAs are done.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(cta_mask)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void proj_drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
@@ -124,7 +92,7 @@ __device__ __forceinline__ void proj_drain_wait(uint32_t bar, uint32_t parity, u
     }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
+__global__ void __launch_bounds__(kProjThreads, 1)
     qkv_proj_fp8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                         const ProjParams p) {
     using T = ProjTraits;
@@ -140,14 +108,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nk = p.n_kblocks;
-    const int crank = static_cast<int>(cluster_ctarank());   // 0 or 1
-    const int cluster = static_cast<int>(blockIdx.x) >> 1;
-    const int n_clusters = static_cast<int>(gridDim.x) >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < T::STAGES; ++s) {
             mbar_init(bar(PB_FULL + s), 1);
-            mbar_init(bar(PB_EMPTY + s), 2);  // released by the MMAs of both CTAs
+            mbar_init(bar(PB_EMPTY + s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar(PB_ACC + a), 1);
@@ -167,7 +132,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();  // both CTAs' barriers exist before any multicast lands
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl ctl{abort_flag, p.wait_limit_ns, p.status, kTagQkvProj};
@@ -179,19 +143,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             int it = 0;   // position in the smem ring, continuous across tiles
             int last = -1;
             bool ok = true;
-            for (int pr = cluster; pr < p.n_pairs && ok; pr += n_clusters) {
-                const int nt = pr % p.n_tiles_n, mp = pr / p.n_tiles_n;
+            for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x) {
+                const int nt = tile % p.n_tiles_n, mt = tile / p.n_tiles_n;
                 const int part = nt / p.tiles_per_part, ntile = nt - part * p.tiles_per_part;
-                const int wrow = part * p.inner + p.wrow0 + ntile * T::BN + crank * (T::BN / 2);
-                const int m0 = (2 * mp + crank) * T::BM;
+                const int wrow = part * p.inner + p.wrow0 + ntile * T::BN;
+                const int m0 = mt * T::BM;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % T::STAGES, u = it / T::STAGES;
                     if (u > 0 && !mbar_wait(bar(PB_EMPTY + s), (u - 1) & 1, ctl, 1)) { ok = false; break; }
                     mbar_arrive_expect_tx(bar(PB_FULL + s), T::A_BYTES + T::B_BYTES);
                     tma_load_2d(sA + s * T::A_BYTES, &tmX, bar(PB_FULL + s), kb * T::BK, m0);
-                    // my half of the weight rows, into the same offset of both CTAs
-                    tma_load_2d_mc(sB + s * T::B_BYTES + crank * (T::B_BYTES / 2), &tmW, bar(PB_FULL + s),
-                                   kb * T::BK, wrow, 0x3);
+                    tma_load_2d(sB + s * T::B_BYTES, &tmW, bar(PB_FULL + s), kb * T::BK, wrow);
                     last = it;
                 }
             }
@@ -208,7 +170,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
             constexpr uint64_t kStageA = T::A_BYTES >> 4, kStageB = T::B_BYTES >> 4;
             bool ok = true;
             int it = 0, n_local = 0;
-            for (int pr = cluster; pr < p.n_pairs && ok; pr += n_clusters, ++n_local) {
+            for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++n_local) {
                 const int acc = n_local & 1, use = n_local >> 1;
                 if (use > 0 && !mbar_wait(bar(PB_ACCFREE + acc), (use - 1) & 1, ctl, 11)) { ok = false; break; }
                 tc_fence_after_sync();
@@ -221,7 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
                     for (int kk = 0; kk < T::BK / 32; ++kk)  // K = 32 bytes per MMA
                         mma_f8(d, dA + s * kStageA + kk * 2, dB + s * kStageB + kk * 2, T::IDESC,
                                (kb > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit_mc(bar(PB_EMPTY + s), 0x3);  // this stage may be refilled in both CTAs
+                    mma_commit(bar(PB_EMPTY + s));  // this stage may be refilled
                 }
                 if (ok) mma_commit(bar(PB_ACC + acc));
             }
@@ -235,11 +197,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
         const int wq = warp & 3;  // TMEM lane quarter of this warp
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         int n_local = 0;
-        for (int pr = cluster; pr < p.n_pairs; pr += n_clusters, ++n_local) {
+        for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++n_local) {
             const int acc = n_local & 1, use = n_local >> 1;
             if (!__all_sync(0xffffffffu, mbar_wait(bar(PB_ACC + acc), use & 1, ctl, 20))) break;
             tc_fence_after_sync();
-            const int nt = pr % p.n_tiles_n, mt = 2 * (pr / p.n_tiles_n) + crank;
+            const int nt = tile % p.n_tiles_n, mt = tile / p.n_tiles_n;
             const int part = nt / p.tiles_per_part, ntile = nt - part * p.tiles_per_part;
             const int row = mt * T::BM + wq * 32 + lane;
             __nv_bfloat16* base = part == 0 ? p.out[0] : (part == 1 ? p.out[1] : p.out[2]);
@@ -276,7 +238,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();  // the partner no longer multicasts into this CTA or arrives on its barriers
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<512>(tmem);
@@ -303,7 +264,7 @@ int launch_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, 
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(hidden), static_cast<cuuint64_t>(3) * inner};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(hidden)};
-        const cuuint32_t box[2] = {T::BK, T::BN / 2};  // each CTA of a pair loads half of the weight rows
+        const cuuint32_t box[2] = {T::BK, T::BN};
         const cuuint32_t estr[2] = {1, 1};
         int rc = encode_tensor_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, w, dims, strides, box, estr,
                                    CU_TENSOR_MAP_SWIZZLE_128B);
@@ -320,7 +281,7 @@ int launch_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, 
     prm.n_kblocks = (hidden + T::BK - 1) / T::BK;
     prm.tiles_per_part = (prm.Nr + T::BN - 1) / T::BN;
     prm.n_tiles_n = 3 * prm.tiles_per_part;
-    prm.n_pairs = prm.n_tiles_n * (((S + T::BM - 1) / T::BM + 1) / 2);
+    prm.n_tiles = prm.n_tiles_n * ((S + T::BM - 1) / T::BM);
     prm.scale = scale;
     prm.wait_limit_ns = wait_limit_ns();
     int rc = device_status_ptr(&prm.status);
@@ -332,7 +293,7 @@ int launch_qkv_proj_fp8(const void* x, const void* w, float scale, void* q_out, 
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    const unsigned grid = 2u * static_cast<unsigned>(min(prm.n_pairs, n_sm / 2));  // whole clusters
+    const unsigned grid = static_cast<unsigned>(min(prm.n_tiles, n_sm));
     qkv_proj_fp8_kernel<<<grid, kProjThreads, T::SMEM_BYTES, stream>>>(mx, mw, prm);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e);

@@ -79,7 +79,8 @@ enum h3attn_status {
  *               results (test aid).
  *   w_q, w_k    [D] fp32 norm weights (shared by all heads).
  *   pos         [S][3] int32 (t, h, w) positions, shared by all batch items.
- *   d_t+d_h+d_w == D, each even.  eps >= 0, theta > 0.
+ *   d_t+d_h+d_w == D, each even.  eps >= 0, theta > 0.  1 <= H <= 65535,
+ *   B * S < 2^31 (H3ATTN_ERR_SHAPE otherwise).
  */
 H3ATTN_API int h3attn_qk_norm_rope(const void* q, const void* k, void* q_out, void* k_out, float* dbg_fp32,
                         const float* w_q, const float* w_k, const int32_t* pos, int B, int S, int H, int D,
@@ -96,7 +97,8 @@ H3ATTN_API int h3attn_qk_norm_rope(const void* q, const void* k, void* q_out, vo
  *   qh_out,kh_out [P][S][H/P][D] bf16, bit-identical to
  *                 seq2head(qk_norm_rope(q, k)); must not overlap q or k.
  *   dbg_fp32      NULL, or [2][S][H][D] fp32 (token-major, unrounded q then k).
- *   S % P == 0, H % P == 0; other arguments as h3attn_qk_norm_rope.
+ *   S % P == 0, H % P == 0, 1 <= H <= 65535, S * H * D / 8 < 2^32; other
+ *   arguments as h3attn_qk_norm_rope.
  */
 H3ATTN_API int h3attn_qk_norm_rope_seq2head(const void* q, const void* k, void* qh_out, void* kh_out,
                                             float* dbg_fp32, const float* w_q, const float* w_k,
@@ -119,6 +121,8 @@ H3ATTN_API int h3attn_qk_norm_rope_seq2head(const void* q, const void* k, void* 
  *
  *   q, k, v, o  [B][S][H_buf][D] bf16; o must not overlap q, k or v.
  *   kv_len      HOST array [B] with 1 <= kv_len[b] <= S, or NULL for all S.
+ *               It is read on the host during the call; a device pointer is
+ *               refused with H3ATTN_ERR_ARG before it is touched.
  *               Rows >= kv_len[b] of k and v are never read (NaN there is fine).
  *   scale       softmax scale; <= 0 selects 1/sqrt(D).
  * The per-head result does not depend on head_begin/head_count or on how many
@@ -184,21 +188,25 @@ H3ATTN_API int h3attn_qkv_proj_fp8(const void* x, const void* w, float scale, vo
                                    void* v_out, int S, int hidden, int inner, int P, int rank, void* stream);
 
 /*
- * h3attn_get_device_status -- synchronise `stream`, then read and clear the
- * device status word of the current device.  Returns H3ATTN_OK,
- * H3ATTN_ERR_DEVICE_TIMEOUT (a kernel gave up on a wait, wrote nothing
- * trustworthy and returned), H3ATTN_ERR_DEVICE_BOUNDS (debug-check builds
- * only: a kernel's index check failed and the access was skipped), or
- * H3ATTN_ERR_CUDA if the synchronisation itself failed.  The first error
- * recorded since the last read wins.
+ * h3attn_get_device_status -- take the device status word of the current
+ * device: a one-thread kernel enqueued on `stream` reads and clears it in one
+ * atomic exchange, then the call synchronises `stream` and returns what it
+ * read.  Returns H3ATTN_OK, H3ATTN_ERR_DEVICE_TIMEOUT (a kernel gave up on a
+ * wait, wrote nothing trustworthy and returned), H3ATTN_ERR_DEVICE_BOUNDS
+ * (debug-check builds only: a kernel's index check failed and the access was
+ * skipped), or H3ATTN_ERR_CUDA if the launch or synchronisation failed.  The
+ * first error recorded since the last take wins.  Errors recorded by kernels
+ * on other streams are reported if they landed before the take, and kept for
+ * the next call otherwise; none is cleared without being returned.  Calls
+ * from several host threads are serialised per device.
  */
 H3ATTN_API int h3attn_get_device_status(void* stream);
 
-/* Diagnostic word recorded with the last device error, 0 if none; read after
- * h3attn_get_device_status.  Kernel tag << 32 | site << 16 | low 16 bits of
- * the block index (timeouts) or of the offending index (bounds checks).
- * Kernel tags: 1 attention, 2 wait self-test, 3 fp8 projection,
- * 4 norm/RoPE, 5 seq2head, 6 head2seq, 7 head2seq_heads. */
+/* Diagnostic word recorded with the last device error taken on the current
+ * device, 0 if none; read after h3attn_get_device_status.  Kernel tag << 32 |
+ * site << 16 | low 16 bits of the block index (timeouts) or of the offending
+ * index (bounds checks).  Kernel tags: 1 attention, 2 wait self-test, 3 fp8
+ * projection, 4 norm/RoPE, 5 seq2head, 6 head2seq, 7 head2seq_heads. */
 H3ATTN_API unsigned long long h3attn_last_device_error_info(void);
 
 /* cudaError_t value behind the most recent H3ATTN_ERR_CUDA on this thread. */

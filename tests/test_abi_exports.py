@@ -126,6 +126,10 @@ def test_argument_checks_run_before_any_cuda_call(lib):
     assert g(*base, 64, 56, 128, 2, 32, 48, 46, 1e-6, 1e4, null) == h3.H3ATTN_ERR_SHAPE      # split != D
     assert g(fake, fake + 0x100000, fake + 0x10, fake + 0x300000, null, fake + 0x400000, fake + 0x500000,
              fake + 0x600000, 64, 56, 128, 2, 32, 48, 48, 1e-6, 1e4, null) == h3.H3ATTN_ERR_ALIAS  # out overlaps q
+    # the head-group reciprocal of the sharded store is exact only below 2^16 heads
+    assert g(*base, 2, 65536, 64, 2, 16, 24, 24, 1e-6, 1e4, null) == h3.H3ATTN_ERR_SHAPE
+    assert f(fake, fake + 0x10000000, fake + 0x20000000, fake + 0x30000000, null, fake + 0x40000000,
+             fake + 0x50000000, fake + 0x60000000, 1, 2, 65536, 64, 16, 24, 24, 1e-6, 1e4, null) == h3.H3ATTN_ERR_SHAPE
     f2 = lib.h3attn_head2seq_heads
     assert f2(fake, fake + 0x1000000, 64, 56, 128, 2, 2, 0, 1, null) == h3.H3ATTN_ERR_SHAPE   # group >= P
     assert f2(fake, fake + 0x1000000, 64, 56, 128, 2, 1, 20, 9, null) == h3.H3ATTN_ERR_SHAPE  # past H/P

@@ -5,7 +5,8 @@ seq2head P=2 -> two 28-head attention launches -> head2seq), compared with
 the fp64 oracle on sampled heads and query rows (the oracle computes each
 sampled row against every valid key); the Ulysses split at P in {2, 4, 7, 8}
 compared bit for bit with one all-heads call, and the permutations bit for
-bit with the oracle's index formula; 1080p (262,144 tokens) on sampled rows.
+bit with the oracle's index formula; 1080p (262,144 tokens) through the same
+step on 4 sampled heads x 512 sampled query rows.
 Inputs are seeded draws on the device (torch's CUDA generator); no oracle
 input comes from the library's kernels.
 """
@@ -99,19 +100,27 @@ def test_480p_ulysses_split_is_bit_identical(h3, cuda_device, P):
     assert torch.equal(back.view(torch.int16), v.view(torch.int16))
 
 
-def test_1080p_matches_oracle_on_sampled_rows(h3, cuda_device):
+def test_1080p_bench_step_matches_oracle_on_sampled_rows(h3, cuda_device):
+    """1080p through the bench's own step (fused QK-norm+RoPE+seq2head, P = 2,
+    two 28-head attention launches, head2seq) on 4 sampled heads -- two from
+    each head group, including the first and the last -- x 512 sampled query
+    rows: the audio/video boundary, the last valid row, padding rows and rows
+    at both edges of 256-row query blocks among them."""
     w = synth.WORKLOADS["1080p"]
     dev = cuda_device
     q, k, v, wq, wk, pos = _inputs(w, dev)
-    qr, kr = torch.empty_like(q), torch.empty_like(k)
-    h3.h3attn_qk_norm_rope(q, k, qr, kr, wq.to(dev), wk.to(dev), torch.from_numpy(pos).to(dev), *w.rope_split,
-                           w.eps, w.theta)
-    heads = [3, 41]
-    full_o = torch.empty_like(q)
-    h3.h3attn_forward(qr, kr, v, full_o, kv_len=w.S_v)   # all 56 heads in one launch
+    o = h3.ulysses_attention_step(q, k, v, wq.to(dev), wk.to(dev), torch.from_numpy(pos).to(dev), 2, w.S_v,
+                                  *w.rope_split, w.eps, w.theta)
     assert h3.h3attn_get_device_status() == 0
-    rows = _sample_rows(w, 24, 9)
+    heads = [0, 27, 28, 55]
+    fixed = [0, 1, 255, 256, w.n_audio - 2, w.n_audio - 1, w.n_audio, w.n_audio + 1, w.S // 2 - 1, w.S // 2,
+             w.S_v - 2, w.S_v - 1, w.S_v, w.S - 1]
+    rng = np.random.default_rng(9)
+    drawn = rng.choice(w.S, 512 + len(fixed), replace=False)
+    sampled = drawn[~np.isin(drawn, fixed)][: 512 - len(fixed)]           # random order kept: no bias
+    rows = np.sort(np.concatenate([sampled, fixed]))
+    assert len(rows) == 512
     ref = _oracle_rows(w, q, k, v, wq, wk, pos, heads, rows)
-    got = full_o[torch.as_tensor(rows, device=dev)][:, heads].float().cpu().numpy()
+    got = o[torch.as_tensor(rows, device=dev)][:, heads].float().cpu().numpy()
     err = np.abs(got - ref).max(axis=(0, 2)) / np.abs(ref).max(axis=(0, 2))
     assert np.all(err <= ATTN_TOL), f"per-head rel err {err}"

@@ -117,6 +117,66 @@ def test_norm_rope_in_place_equals_out_of_place(h3, cuda_device):
     assert torch.equal(q2, qo) and torch.equal(k2, ko)
 
 
+def _check_norm_rope_bars(dbg, outs, refs):
+    for i in range(2):
+        ref = refs[i]
+        err = np.abs(dbg[i] - ref).max() / np.abs(ref).max()
+        assert err <= NORM_TOL, f"fp32 norm/rope rel err {err:.3e} > {NORM_TOL}"
+        got_b = outs[i].cpu()
+        assert torch.equal(got_b.view(torch.int16),
+                           torch.from_numpy(dbg[i]).to(torch.bfloat16).view(torch.int16))
+        got = got_b.double().numpy()
+        ref_b = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref_b), 2.0 ** -126))) - 7)
+        assert np.all(np.abs(got - ref) <= ulp + NORM_TOL * np.abs(ref).max()), "more than one bf16 ulp off"
+
+
+@pytest.mark.parametrize("name", ["480p", "1080p"])
+def test_norm_rope_at_full_size_positions(h3, cuda_device, name):
+    """The fp32 1e-5 and bf16 one-ulp bars at the positions of the full-size
+    packed sequences, where the angles are largest: sampled tokens of the 480p /
+    1080p position layout, including the last audio token (t = 991), the last
+    video token (largest t, h and w of the grid), the audio/video boundary and
+    padding rows, run as a sequence of their own (token-major, and fused with
+    the P = 2 head-sharded store)."""
+    w = synth.WORKLOADS[name]
+    pos_all = synth.packed_positions(w)
+    rng = np.random.default_rng(19)
+    last_row = w.n_audio + (w.grid_h - 1) * w.grid_w      # t = 0, h = max, w = 0
+    fixed = [0, w.n_audio - 1, w.n_audio, w.n_audio + w.grid_w - 1, last_row, w.S_v - w.grid_w, w.S_v - 1,
+             w.S_v, w.S - 1]
+    drawn = rng.choice(w.S, 2048 + len(fixed), replace=False)
+    sampled = drawn[~np.isin(drawn, fixed)][: 2048 - len(fixed)]
+    idx = np.sort(np.concatenate([sampled, fixed]))   # 2048 rows: even, so P = 2 divides
+    pos = np.ascontiguousarray(pos_all[idx])
+    assert pos[:, 0].max() == w.n_audio - 1 and pos[:, 1].max() == w.grid_h - 1 and pos[:, 2].max() == w.grid_w - 1
+    assert (pos[:, 0] == w.frames - 1).any()
+    S = len(idx)
+    shape = (S, w.H, w.D)
+    q, k = synth.randn_bf16(shape, 31), synth.randn_bf16(shape, 32)
+    wq, wk = synth.norm_weights(w.D)
+    dev = cuda_device
+    qd, kd, wqd, wkd, posd = q.to(dev), k.to(dev), wq.to(dev), wk.to(dev), torch.from_numpy(pos).to(dev)
+    refs = [oracle.norm_rope(oracle.bf16_to_f64(t), wt.double().numpy(), pos, w.eps, *w.rope_split, w.theta)
+            for t, wt in ((q, wq), (k, wk))]
+    qo, ko = torch.empty_like(qd), torch.empty_like(kd)
+    dbg = torch.empty((2,) + shape, dtype=torch.float32, device=dev)
+    h3.h3attn_qk_norm_rope(qd, kd, qo, ko, wqd, wkd, posd, *w.rope_split, w.eps, w.theta, dbg_fp32=dbg)
+    assert h3.h3attn_get_device_status() == 0
+    _check_norm_rope_bars(dbg.cpu().numpy(), (qo, ko), refs)
+    # the fused store (the bench's launch) writes the same bits in the head-sharded layout
+    P = 2
+    hs = (P, S, w.H // P, w.D)
+    qh, kh = torch.empty(hs, dtype=torch.bfloat16, device=dev), torch.empty(hs, dtype=torch.bfloat16, device=dev)
+    dbg2 = torch.empty_like(dbg)
+    h3.h3attn_qk_norm_rope_seq2head(qd, kd, qh, kh, wqd, wkd, posd, P, *w.rope_split, w.eps, w.theta,
+                                    dbg_fp32=dbg2)
+    assert h3.h3attn_get_device_status() == 0
+    assert torch.equal(dbg2, dbg)
+    np.testing.assert_array_equal(bits(qh), oracle.seq2head(bits(qo), P))
+    np.testing.assert_array_equal(bits(kh), oracle.seq2head(bits(ko), P))
+
+
 # ---------------------------------------------------------------- attention
 def _attn(h3, dev, S, H, D, kv, seed=21, rows=None, heads=None):
     q, k, v = (synth.randn_bf16((S, H, D), seed + i) for i in range(3))
@@ -282,6 +342,38 @@ def test_host_memory_is_refused_before_any_launch(h3, cuda_device):
     assert h3.h3attn_get_device_status() == 0
 
 
+def test_kv_len_in_device_memory_is_refused(h3, cuda_device):
+    """kv_len is read on the host; a device pointer is refused with
+    H3ATTN_ERR_ARG instead of being dereferenced."""
+    lib = h3.load_library()
+    S, H, D = 256, 2, 64
+    x = torch.zeros((S, H, D), dtype=torch.bfloat16, device=cuda_device)
+    o = torch.zeros_like(x)
+    kv_dev = torch.full((1,), S, dtype=torch.int32, device=cuda_device)
+    st = torch.cuda.current_stream(cuda_device).cuda_stream
+    assert lib.h3attn_forward(x.data_ptr(), x.data_ptr(), x.data_ptr(), o.data_ptr(), 1, S, H, D, 0, H,
+                              kv_dev.data_ptr(), 0.0, st) == h3.H3ATTN_ERR_ARG
+    kv_pinned = torch.full((1,), S, dtype=torch.int32).pin_memory()
+    assert lib.h3attn_forward(x.data_ptr(), x.data_ptr(), x.data_ptr(), o.data_ptr(), 1, S, H, D, 0, H,
+                              kv_pinned.data_ptr(), 0.0, st) == h3.H3ATTN_OK
+    assert h3.h3attn_get_device_status() == 0
+
+
+def test_status_recorded_on_another_stream_is_not_lost(h3, cuda_device):
+    """A device error recorded by a kernel on stream A is reported by a status
+    read on stream B -- now if it landed before the read, otherwise by the
+    next read -- and is cleared only when it has been returned."""
+    a, b = torch.cuda.Stream(cuda_device), torch.cuda.Stream(cuda_device)
+    assert h3.h3attn_get_device_status() == 0
+    h3.h3attn_selftest_wait_timeout(50_000_000, stream=a)      # gives up after 50 ms
+    first = h3.h3attn_get_device_status(stream=b)               # B does not wait for A
+    a.synchronize()
+    second = h3.h3attn_get_device_status(stream=b)
+    assert sorted([first, second]) == [h3.H3ATTN_ERR_DEVICE_TIMEOUT, h3.H3ATTN_OK]
+    assert (h3.h3attn_last_device_error_info() >> 32) == 2
+    assert h3.h3attn_get_device_status(stream=b) == 0
+
+
 # ------------------------------------------------------------- whole path
 @pytest.mark.parametrize("P", [1, 2, 4])
 def test_pipeline_c2_matches_oracle(h3, cuda_device, P):
@@ -364,6 +456,43 @@ def test_chunked_step_bit_identical_for_any_chunk_count(h3, cuda_device):
                 torch.cuda.synchronize()
                 assert torch.equal(o.view(torch.int16), ref.view(torch.int16)), (fused, chunks, xs)
     assert h3.h3attn_get_device_status() == 0
+
+
+@pytest.fixture(scope="module")
+def c2_oracle_sample():
+    """fp64 oracle of the whole path at c2 on sampled heads and rows, from the
+    same seeded CPU inputs the GPU step is given."""
+    w = synth.WORKLOADS["c2"]
+    q, k, v = synth.qkv(w)
+    wq, wk = synth.norm_weights(w.D)
+    pos = synth.packed_positions(w)
+    heads = np.array([0, 13, 27, 28, 41, 55])
+    rows = np.unique(np.concatenate([np.arange(0, w.S, 29), [w.n_audio - 1, w.n_audio, w.S_v - 1, w.S_v, w.S - 1]]))
+    qf = oracle.norm_rope(oracle.bf16_to_f64(q)[:, heads], wq.double().numpy(), pos, w.eps, *w.rope_split, w.theta)
+    kf = oracle.norm_rope(oracle.bf16_to_f64(k)[:, heads], wk.double().numpy(), pos, w.eps, *w.rope_split, w.theta)
+    ref = oracle.attention(qf[rows], kf, oracle.bf16_to_f64(v)[:, heads], kv_len=w.S_v)
+    return (q, k, v, wq, wk, pos), heads, rows, ref
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_chunked_step_matches_oracle(h3, cuda_device, c2_oracle_sample, fused):
+    """The head-chunked step (each group's heads in 2, 4 or 8 attention launches,
+    the output exchange of each chunk on the launching stream or on a second
+    stream) against the fp64 oracle on the same seeded inputs."""
+    (q, k, v, wq, wk, pos), heads, rows, ref = c2_oracle_sample
+    w = synth.WORKLOADS["c2"]
+    dev = cuda_device
+    args = (q.to(dev), k.to(dev), v.to(dev), wq.to(dev), wk.to(dev), torch.from_numpy(pos).to(dev), 2, w.S_v,
+            *w.rope_split, w.eps, w.theta)
+    side = torch.cuda.Stream(dev)
+    for chunks in (2, 4, 8):
+        for xs in (None, side):
+            o = h3.ulysses_attention_step(*args, fused=fused, attn_chunks=chunks, exchange_stream=xs)
+            torch.cuda.synchronize()
+            assert h3.h3attn_get_device_status() == 0
+            got = o.float().cpu().numpy()[rows][:, heads]
+            err = per_head_rel_err(got, ref)
+            assert np.all(err <= ATTN_TOL), f"chunks={chunks}, second stream={xs is not None}: {err}"
 
 
 def test_head2seq_heads_writes_only_its_heads(h3, cuda_device):

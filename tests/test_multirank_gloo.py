@@ -1,8 +1,13 @@
-"""Multi-rank host logic of bench.py on CPU with the gloo backend (world size 2).
+"""Multi-rank logic on CPU with the gloo backend.
 
-Each rank runs an independent sequence; the only cross-rank steps are the
-barrier and the max-over-ranks timing used for the whole-job throughput, and
-the reference arm prints from rank 0 only.  No GPU needed."""
+bench.py across ranks (world size 2): each rank runs an independent sequence;
+the only cross-rank steps are the barrier and the max-over-ranks timing used
+for the whole-job throughput, and the reference arm prints from rank 0 only.
+
+The Ulysses exchange across ranks (world size 2 and 4): the product's
+all-to-all wiring moves each rank's rows to the rank that owns their heads
+and the output rows back, checked bit for bit against the single-process
+layout and result.  No GPU needed."""
 import json
 import os
 import socket
@@ -67,3 +72,90 @@ def test_reference_arm_under_torchrun_prints_once_from_rank0():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["cpu_baseline"]["kind"] == "oracle"
     assert d["unit"] == "TFLOP/s" and d["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+# ------------------------------------------------ Ulysses exchange across ranks
+def _ulysses_worker(rank, world, port, out):
+    """Rank `rank` of a Ulysses group of `world` on CPU tensors (gloo).
+
+    The per-token and attention arithmetic are the fp64 oracle's (rounded to
+    bf16 where the GPU path stores bf16); what is under test is the product's
+    exchange: which rows of which heads reach which rank, in which order."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import torch
+
+    import oracle
+    from dit_sequence_attention_gb300 import synth
+    from dit_sequence_attention_gb300.ulysses import UlyssesGroup
+
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        P = world
+        S, H, D, kv = 512, 8, 64, 480              # 32 padding keys at the end (in the last rank's shard)
+        split = (16, 24, 24)
+        S_loc = S // P
+        q, k, v = (synth.randn_bf16((S, H, D), 300 + i) for i in range(3))
+        wq, wk = synth.norm_weights(D)
+        pos = synth.packed_positions(synth.WORKLOADS["tiny"])
+        pos = np.concatenate([pos, pos])[:S]         # any position triples will do
+        rows = slice(rank * S_loc, (rank + 1) * S_loc)
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16)
+
+        def words(t):
+            return oracle.bf16_bits(t)
+
+        # this rank's per-token work on its own rows, packed in the exchange's chunk order
+        qr = bf16(oracle.norm_rope(oracle.bf16_to_f64(q[rows]), wq.double().numpy(), pos[rows], 1e-6, *split))
+        kr = bf16(oracle.norm_rope(oracle.bf16_to_f64(k[rows]), wk.double().numpy(), pos[rows], 1e-6, *split))
+        sends = [torch.from_numpy(oracle.seq2head(words(t), P).view(np.int16)).view(torch.bfloat16)
+                 for t in (qr, kr, v[rows].contiguous())]
+        ug = UlyssesGroup()
+        assert (ug.P, ug.rank) == (P, rank)
+        recv = [ug.exchange(s) for s in sends]
+
+        # single-process reference: the whole sequence on one rank
+        qf = bf16(oracle.norm_rope(oracle.bf16_to_f64(q), wq.double().numpy(), pos, 1e-6, *split))
+        kf = bf16(oracle.norm_rope(oracle.bf16_to_f64(k), wk.double().numpy(), pos, 1e-6, *split))
+        heads_ok = all(np.array_equal(words(r).reshape(S, H // P, D), oracle.seq2head(words(f), P)[rank])
+                       for r, f in zip(recv, (qf, kf, v)))
+
+        # attention of this rank's head group, then the output exchange back to the row owners
+        grp = [oracle.bf16_to_f64(r.view(S, H // P, D)) for r in recv]
+        o_group = bf16(oracle.attention(*grp, kv_len=kv)).view(P, S_loc, H // P, D)
+        o_back = ug.exchange(o_group)
+        o_shard = oracle.head2seq(words(o_back), P)
+        o_full = bf16(oracle.attention(oracle.bf16_to_f64(qf), oracle.bf16_to_f64(kf), oracle.bf16_to_f64(v),
+                                       kv_len=kv))
+        out[rank] = (heads_ok, bool(np.array_equal(o_shard, words(o_full)[rows])))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_ulysses_exchange_across_ranks_gloo(world):
+    """World size 2 and 4: after the sequence->heads exchange every rank holds
+    exactly the single-process seq2head group of its heads (bit for bit), and
+    after attention and the heads->sequence exchange every rank holds exactly
+    its rows of the single-process output."""
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_ulysses_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    assert sorted(res) == list(range(world))
+    for r in range(world):
+        heads_ok, out_ok = res[r]
+        assert heads_ok, f"rank {r}: exchanged head-group buffers differ from seq2head of the whole sequence"
+        assert out_ok, f"rank {r}: output rows differ from the single-process result"
+
+
+def test_ulysses_exchange_rejects_mismatched_buffers():
+    import torch
+    from dit_sequence_attention_gb300.ulysses import _words
+    with pytest.raises(ValueError):
+        _words(torch.zeros((2, 3), dtype=torch.float32))
+    with pytest.raises(ValueError):
+        _words(torch.zeros((2, 3), dtype=torch.bfloat16))

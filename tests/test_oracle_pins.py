@@ -54,6 +54,21 @@ def test_rope_worked_example():
     np.testing.assert_allclose(y.reshape(-1), g["y"], rtol=0, atol=1e-15)
 
 
+def test_norm_rope_worked_example():
+    """QK-norm (weight applied to the normalised value) and then RoPE, against a
+    hand-worked case whose weights differ inside each rotation pair, so that
+    rotating before weighting, or weighting after the rotation, fails."""
+    g, _ = read_golden("norm_rope_worked_example.txt")
+    D = int(g["D"][0])
+    d_t, d_h, d_w = (int(v) for v in g["split"])
+    x = np.array(g["x"]).reshape(1, 1, D)
+    w = np.array(g["w"])
+    pos = np.array([g["pos"]], dtype=np.int32)
+    for eps_key, y_key in (("eps_half", "y_eps_half"), ("eps_zero", "y_eps_zero")):
+        y = oracle.norm_rope(x, w, pos, g[eps_key][0], d_t, d_h, d_w, g["theta"][0])
+        np.testing.assert_allclose(y.reshape(-1), g[y_key], rtol=0, atol=1e-14)
+
+
 def test_rope_zero_position_is_identity():
     x = RNG.standard_normal((9, 3, 128))
     pos = np.zeros((9, 3), dtype=np.int32)
