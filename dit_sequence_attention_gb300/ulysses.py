@@ -20,8 +20,8 @@ arrives gives this rank's [S/P][H][D] output shard.
 
 The exchanges move whole bf16 rows as 32-bit words (bit-exact; the element
 types every backend supports), with NCCL on GPUs and gloo on CPU tensors.
-Every buffer handed to a collective is memory of this rank's own device; no
-multicast or NVLink-SHARP path is used (set ``NCCL_NVLS_ENABLE=0`` before the
+Every buffer handed to a collective is memory of this rank's own device; the
+collectives are plain point-to-point transfers (set ``NCCL_NVLS_ENABLE=0`` before the
 process group is created).
 """
 from __future__ import annotations
