@@ -18,6 +18,18 @@ through the same exchange: the group output [S][H/P][D] seen as
 [P][S/P][H/P][D] sends rank g its own rows, and ``h3attn_head2seq`` of what
 arrives gives this rank's [S/P][H][D] output shard.
 
+The all-gather variant (same README section: for world sizes up to 4 the
+modulated hidden state is gathered instead, and every rank projects all rows
+through only its own head rows of qkv_proj -- exact because the fp8 weight has
+one scale per tensor): ``gather_rows`` collects the fp8 hidden rows of every
+rank, ``project`` runs ``h3attn_qkv_proj_fp8`` for this rank's heads straight
+into the head-group buffers, ``norm_rope_group`` applies the QK-norm and RoPE
+there (per token and head, so with all rows' positions), and attention and the
+output exchange follow as in the all-to-all form.  Both forms give
+bit-identical outputs: the projection of one (row, output column) and the
+per-row norm / rotation / attention do not depend on how rows and heads are
+split.
+
 The exchanges move whole bf16 rows as 32-bit words (bit-exact; the element
 types every backend supports), with NCCL on GPUs and gloo on CPU tensors.
 Every buffer handed to a collective is memory of this rank's own device; the
@@ -77,13 +89,32 @@ class UlyssesGroup:
         dist.all_to_all_single(_words(recv), _words(send), group=self.group)
         return recv
 
-    def make_workspace(self, S_local: int, H: int, D: int, device) -> dict:
-        """Buffers of one distributed step (allocated once by the caller)."""
+    def make_workspace(self, S_local: int, H: int, D: int, device, hidden: int | None = None) -> dict:
+        """Buffers of one distributed step (allocated once by the caller);
+        `hidden` adds the gathered fp8 hidden state of the all-gather form."""
         P = self.P
         e = dict(dtype=torch.bfloat16, device=device)
         shape = (P, S_local, H // P, D)
-        return {name: torch.empty(shape, **e) for name in ("qs", "ks", "vs", "qh", "kh", "vh", "oh", "os")} | \
-            {"o": torch.empty((S_local, H, D), **e)}
+        work = {name: torch.empty(shape, **e) for name in ("qs", "ks", "vs", "qh", "kh", "vh", "oh", "os")}
+        work["o"] = torch.empty((S_local, H, D), **e)
+        if hidden is not None:
+            work["x"] = torch.empty((P * S_local, hidden), dtype=torch.uint8, device=device)
+        return work
+
+    def gather_rows(self, x_local: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+        """All-gather of this rank's rows [S/P][...] into [S][...] in rank order
+        (the fp8 hidden state of the all-gather form, as uint8 codes)."""
+        if not self.has_group:
+            raise RuntimeError("this UlyssesGroup was made without a process group; it cannot exchange")
+        x_local = x_local.contiguous()
+        if out is None:
+            out = torch.empty((self.P * x_local.shape[0],) + tuple(x_local.shape[1:]), dtype=x_local.dtype,
+                              device=x_local.device)
+        elif out.shape[0] != self.P * x_local.shape[0] or out.shape[1:] != x_local.shape[1:] or \
+                out.dtype != x_local.dtype or out.device != x_local.device:
+            raise ValueError("out must be [P * rows, ...] of the same dtype and device as x_local")
+        dist.all_gather_into_tensor(out, x_local, group=self.group)
+        return out
 
     def pack(self, q, k, v, w_q, w_k, pos, d_t, d_h, d_w, eps, theta, work, stream):
         """Per-token work on this rank's rows, written in the exchange's chunk
@@ -92,6 +123,24 @@ class UlyssesGroup:
         h3attn_qk_norm_rope_seq2head(q, k, work["qs"], work["ks"], w_q, w_k, pos, self.P, d_t, d_h, d_w, eps, theta,
                                      stream=stream)
         h3attn_seq2head(v, work["vs"], self.P, stream)
+
+    def project(self, x_full, w_fp8, scale, work, stream):
+        """All-gather form: q, k, v of this rank's heads for every row, as the
+        head-group buffers [S][H/P][D]: the gathered hidden state [S][hidden]
+        (E4M3 codes) through this rank's head rows of qkv_proj
+        ([3 * inner][hidden] E4M3, q then k then v rows), times `scale`."""
+        from . import h3attn_qkv_proj_fp8
+        h3attn_qkv_proj_fp8(x_full, w_fp8, scale, work["qh"], work["kh"], work["vh"], self.P, self.rank,
+                            stream=stream)
+
+    def norm_rope_group(self, w_q, w_k, pos, d_t, d_h, d_w, eps, theta, work, stream):
+        """All-gather form: QK-norm and RoPE in place on the head-group buffers
+        (every row, this rank's heads; `pos` holds all S rows' positions)."""
+        from . import h3attn_qk_norm_rope
+        P, S_loc, Hp, D = work["qh"].shape
+        grp = lambda t: t.view(P * S_loc, Hp, D)
+        h3attn_qk_norm_rope(grp(work["qh"]), grp(work["kh"]), grp(work["qh"]), grp(work["kh"]), w_q, w_k, pos,
+                            d_t, d_h, d_w, eps, theta, stream=stream)
 
     def attend(self, kv_len, work, stream):
         """Exact attention of this rank's head group over the whole sequence
@@ -131,6 +180,40 @@ class UlyssesGroup:
         with torch.cuda.stream(stream):
             for src, dst in (("qs", "qh"), ("ks", "kh"), ("vs", "vh")):
                 self.exchange(work[src], work[dst])
+        self.attend(kv_len, work, stream)
+        with torch.cuda.stream(stream):
+            self.exchange(work["oh"], work["os"])
+        return self.unpack(work, stream)
+
+    def attention_step_allgather(self, x_local, w_fp8, scale, w_q, w_k, pos, kv_len, d_t, d_h, d_w, eps=1e-6,
+                                 theta=10000.0, work=None, stream=None):
+        """One step of this rank in the all-gather form.
+
+        x_local  [S/P][hidden] E4M3 codes (uint8): this rank's rows of the
+                 modulated hidden state.
+        w_fp8    [3 * H * D][hidden] E4M3 codes of qkv_proj; `scale` the
+                 product of the two per-tensor scales.
+        pos      [S][3] int32: the positions of ALL rows (every rank computes
+                 attention over the whole sequence for its heads).
+        kv_len   valid keys of the whole sequence.
+        Returns this rank's output rows [S/P][H][D], bit-identical to the
+        all-to-all form fed with the same projection.
+        """
+        P = self.P
+        S_loc, hidden = x_local.shape
+        inner = w_fp8.shape[0] // 3
+        D = w_q.numel()
+        H = inner // D
+        if inner % D or H % P or S_loc % P:
+            raise ValueError(f"P={P} must divide H={H} and the shard length S/P={S_loc}")
+        if work is None:
+            work = self.make_workspace(S_loc, H, D, x_local.device, hidden=hidden)
+        if stream is None:
+            stream = torch.cuda.current_stream(x_local.device)
+        with torch.cuda.stream(stream):
+            self.gather_rows(x_local, work["x"])
+        self.project(work["x"], w_fp8, scale, work, stream)
+        self.norm_rope_group(w_q, w_k, pos, d_t, d_h, d_w, eps, theta, work, stream)
         self.attend(kv_len, work, stream)
         with torch.cuda.stream(stream):
             self.exchange(work["oh"], work["os"])

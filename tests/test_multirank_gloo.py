@@ -4,10 +4,11 @@ bench.py across ranks (world size 2): each rank runs an independent sequence;
 the only cross-rank steps are the barrier and the max-over-ranks timing used
 for the whole-job throughput, and the reference arm prints from rank 0 only.
 
-The Ulysses exchange across ranks (world size 2 and 4): the product's
+The Ulysses exchanges across ranks (world size 2 and 4): the product's
 all-to-all wiring moves each rank's rows to the rank that owns their heads
 and the output rows back, checked bit for bit against the single-process
-layout and result.  No GPU needed."""
+layout and result; the all-gather form gives exactly the all-to-all result.
+No GPU needed."""
 import json
 import os
 import socket
@@ -159,3 +160,90 @@ def test_ulysses_exchange_rejects_mismatched_buffers():
         _words(torch.zeros((2, 3), dtype=torch.float32))
     with pytest.raises(ValueError):
         _words(torch.zeros((2, 3), dtype=torch.bfloat16))
+
+
+# ------------------------------------- all-gather form vs all-to-all form
+def _allgather_worker(rank, world, port, out):
+    """Rank `rank`: the same step through the two exchange forms of the README
+    ("How it works"), the oracle standing in for the kernels.  All-to-all:
+    project this rank's rows through all heads, norm/RoPE, exchange, attend,
+    exchange back.  All-gather: gather every rank's fp8 hidden rows, project
+    all rows through this rank's head rows, norm/RoPE, attend, exchange back."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import torch
+
+    import oracle
+    from dit_sequence_attention_gb300 import synth
+    from dit_sequence_attention_gb300.ulysses import UlyssesGroup
+
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        P = world
+        S, H, D, hidden, kv = 256, 8, 64, 96, 230
+        inner = H * D
+        split = (16, 24, 24)
+        S_loc = S // P
+        rows = slice(rank * S_loc, (rank + 1) * S_loc)
+        x = synth.fp8_e4m3_codes((S, hidden), 51, 1.0)
+        w = synth.fp8_e4m3_codes((3 * inner, hidden), 52, 4.0)
+        scale = 1.0 / (4.0 * hidden ** 0.5)
+        wq, wk = synth.norm_weights(D)
+        pos = synth.packed_positions(synth.WORKLOADS["tiny"])[:S]
+        ug = UlyssesGroup()
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16)
+
+        def nr(t, wt, p):
+            return bf16(oracle.norm_rope(oracle.bf16_to_f64(t), wt.double().numpy(), p, 1e-6, *split))
+
+        def words(t):
+            return oracle.bf16_bits(t)
+
+        def to_bf16_tensor(u16):
+            return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16)
+
+        # all-to-all form
+        loc = oracle.qkv_proj_fp8(x[rows].numpy(), w.numpy(), scale, inner, 1, 0)        # [S/P, 3, inner]
+        q_l, k_l, v_l = (bf16(loc[:, i]).view(S_loc, H, D) for i in range(3))
+        q_l, k_l = nr(q_l, wq, pos[rows]), nr(k_l, wk, pos[rows])
+        sends = [to_bf16_tensor(oracle.seq2head(words(t), P)) for t in (q_l, k_l, v_l)]
+        qa, ka, va = (ug.exchange(s_).view(S, H // P, D) for s_ in sends)
+
+        # all-gather form
+        xg = ug.gather_rows(x[rows])
+        gathered_ok = torch.equal(xg, x)
+        grp = oracle.qkv_proj_fp8(xg.numpy(), w.numpy(), scale, inner, P, rank)          # [S, 3, inner/P]
+        qg, kg, vg = (bf16(grp[:, i]).view(S, H // P, D) for i in range(3))
+        qg, kg = nr(qg, wq, pos), nr(kg, wk, pos)
+        same_inputs = all(torch.equal(a.view(torch.int16), b.view(torch.int16))
+                          for a, b in ((qa, qg), (ka, kg), (va, vg)))
+
+        def finish(q_, k_, v_):
+            o_g = bf16(oracle.attention(oracle.bf16_to_f64(q_), oracle.bf16_to_f64(k_), oracle.bf16_to_f64(v_),
+                                        kv_len=kv)).view(P, S_loc, H // P, D)
+            return oracle.head2seq(words(ug.exchange(o_g)), P)
+
+        out[rank] = (gathered_ok, same_inputs, bool(np.array_equal(finish(qa, ka, va), finish(qg, kg, vg))))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_allgather_form_equals_alltoall_form_gloo(world):
+    """README "How it works": the all-gather exchange gives exactly the
+    all-to-all result.  World size 2 and 4: the gathered hidden rows equal the
+    whole hidden state, both forms hand attention bit-identical head-group
+    q, k, v, and every rank's output rows are bit-identical."""
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_allgather_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    assert sorted(res) == list(range(world))
+    for r in range(world):
+        gathered_ok, same_inputs, same_out = res[r]
+        assert gathered_ok, f"rank {r}: gathered hidden rows differ from the whole hidden state"
+        assert same_inputs, f"rank {r}: the two forms give attention different q/k/v"
+        assert same_out, f"rank {r}: all-gather and all-to-all outputs differ"
