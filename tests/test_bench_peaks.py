@@ -35,3 +35,36 @@ def test_incomplete_or_broken_file_falls_back(tmp_path):
 def test_absent_file_falls_back(tmp_path):
     peaks, src = bench.load_peaks(str(tmp_path / "none.json"))
     assert src == "fallback" and peaks == bench.FALLBACK_PEAKS
+
+
+def _traffic_file(tmp_path, fingerprint, traffic="1625250000"):
+    p = tmp_path / "traffic.txt"
+    p.write_text("attn traffic summary\n"
+                 "  indented: lines are ignored\n"
+                 f"traffic_bytes_per_launch_480p_group28: {traffic}\n"
+                 f"attention_sources_sha256_16: {fingerprint}\n")
+    return str(p)
+
+
+def test_traffic_reported_only_for_the_captured_sources(tmp_path, monkeypatch):
+    """The committed DRAM capture is reported only while the attention sources
+    still have the fingerprint recorded with it; otherwise traffic is null."""
+    fp = bench.attention_fingerprint()
+    assert len(fp) == 16 and int(fp, 16) >= 0
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", _traffic_file(tmp_path, fp))
+    traffic, src = bench.read_traffic()
+    assert traffic == 1625250000.0 and "same kernel sources" in src
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", _traffic_file(tmp_path, "0" * 16))
+    traffic, src = bench.read_traffic()
+    assert traffic is None and "other attention sources" in src
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", _traffic_file(tmp_path, fp, traffic="n/a"))
+    assert bench.read_traffic() == (None, None)
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "absent.txt"))
+    assert bench.read_traffic() == (None, None)
+
+
+def test_committed_traffic_capture_matches_the_current_sources():
+    """The committed capture was taken on the attention sources as they are:
+    if the kernel changes, the capture has to be taken again."""
+    traffic, src = bench.read_traffic()
+    assert traffic is not None and traffic > 4 * 51200 * 28 * 128 * 2, src

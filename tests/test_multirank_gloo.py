@@ -247,3 +247,23 @@ def test_allgather_form_equals_alltoall_form_gloo(world):
         assert gathered_ok, f"rank {r}: gathered hidden rows differ from the whole hidden state"
         assert same_inputs, f"rank {r}: the two forms give attention different q/k/v"
         assert same_out, f"rank {r}: all-gather and all-to-all outputs differ"
+
+
+def test_ulysses_group_without_process_group():
+    """UlyssesGroup(P=, rank=) describes a rank with no process group: its
+    compute phases exist, its exchanges refuse; bad ranks and mismatched
+    buffers are refused."""
+    import torch
+    from dit_sequence_attention_gb300.ulysses import UlyssesGroup
+    g = UlyssesGroup(P=4, rank=3)
+    assert (g.P, g.rank, g.has_group) == (4, 3, False)
+    work = g.make_workspace(8, 8, 64, "cpu", hidden=32)
+    assert work["qs"].shape == (4, 8, 2, 64) and work["o"].shape == (8, 8, 64) and work["x"].shape == (32, 32)
+    assert work["x"].dtype == torch.uint8
+    with pytest.raises(RuntimeError):
+        g.exchange(work["qs"])
+    with pytest.raises(RuntimeError):
+        g.gather_rows(torch.zeros((8, 32), dtype=torch.uint8))
+    for bad in (-1, 4):
+        with pytest.raises(ValueError):
+            UlyssesGroup(P=4, rank=bad)
