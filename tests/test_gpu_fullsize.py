@@ -2,8 +2,8 @@
 
 480p (51,200 tokens, 56 x 128) through the exact bench step (QK-norm+RoPE ->
 seq2head P=2 -> two 28-head attention launches -> head2seq), compared with
-the fp64 oracle on sampled heads and query rows (the oracle computes each
-sampled row against every valid key); the Ulysses split at P in {2, 4, 7, 8}
+the fp64 oracle on 4 sampled heads x 512 sampled query rows (the oracle
+computes each sampled row against every valid key); the Ulysses split at P in {2, 4, 7, 8}
 compared bit for bit with one all-heads call, and the permutations bit for
 bit with the oracle's index formula; 1080p (262,144 tokens) through the same
 step on 4 sampled heads x 512 sampled query rows.
@@ -51,13 +51,23 @@ def _oracle_rows(w, q, k, v, wq, wk, pos, heads, rows):
     return oracle.attention(qr, kr, vs, kv_len=w.S_v)
 
 
-def _sample_rows(w, n, seed):
+def _sample_rows_with_edges(w, n, seed):
+    """n distinct query rows: the edges that matter (first rows, both sides of
+    256-row query blocks and of the sequence middle, the audio/video boundary,
+    the last valid rows, padding rows) plus uniformly drawn ones."""
+    fixed = [0, 1, 255, 256, w.n_audio - 2, w.n_audio - 1, w.n_audio, w.n_audio + 1, w.S // 2 - 1, w.S // 2,
+             w.S_v - 2, w.S_v - 1, w.S_v, w.S - 1]
     rng = np.random.default_rng(seed)
-    fixed = [0, 1, w.n_audio - 1, w.n_audio, w.S_v - 1, w.S_v, w.S - 1]
-    return np.unique(np.concatenate([rng.choice(w.S, n, replace=False), fixed]))
+    drawn = rng.choice(w.S, n + len(fixed), replace=False)
+    sampled = drawn[~np.isin(drawn, fixed)][: n - len(fixed)]           # random order kept: no bias
+    rows = np.sort(np.concatenate([sampled, fixed]))
+    assert len(rows) == n and len(np.unique(rows)) == n
+    return rows
 
 
 def test_480p_bench_step_matches_oracle_on_sampled_rows(h3, cuda_device):
+    """480p through the bench's own step on 4 sampled heads (two per head
+    group, the first and the last among them) x 512 sampled query rows."""
     w = synth.WORKLOADS["480p"]
     q, k, v, wq, wk, pos = _inputs(w, cuda_device)
     dev = cuda_device
@@ -65,7 +75,7 @@ def test_480p_bench_step_matches_oracle_on_sampled_rows(h3, cuda_device):
                                   *w.rope_split, w.eps, w.theta)
     assert h3.h3attn_get_device_status() == 0
     heads = [0, 27, 28, 55]
-    rows = _sample_rows(w, 40, 5)
+    rows = _sample_rows_with_edges(w, 512, 5)
     ref = _oracle_rows(w, q, k, v, wq, wk, pos, heads, rows)
     got = o[torch.as_tensor(rows, device=dev)][:, heads].float().cpu().numpy()
     err = np.abs(got - ref).max(axis=(0, 2)) / np.abs(ref).max(axis=(0, 2))
@@ -113,13 +123,7 @@ def test_1080p_bench_step_matches_oracle_on_sampled_rows(h3, cuda_device):
                                   *w.rope_split, w.eps, w.theta)
     assert h3.h3attn_get_device_status() == 0
     heads = [0, 27, 28, 55]
-    fixed = [0, 1, 255, 256, w.n_audio - 2, w.n_audio - 1, w.n_audio, w.n_audio + 1, w.S // 2 - 1, w.S // 2,
-             w.S_v - 2, w.S_v - 1, w.S_v, w.S - 1]
-    rng = np.random.default_rng(9)
-    drawn = rng.choice(w.S, 512 + len(fixed), replace=False)
-    sampled = drawn[~np.isin(drawn, fixed)][: 512 - len(fixed)]           # random order kept: no bias
-    rows = np.sort(np.concatenate([sampled, fixed]))
-    assert len(rows) == 512
+    rows = _sample_rows_with_edges(w, 512, 9)
     ref = _oracle_rows(w, q, k, v, wq, wk, pos, heads, rows)
     got = o[torch.as_tensor(rows, device=dev)][:, heads].float().cpu().numpy()
     err = np.abs(got - ref).max(axis=(0, 2)) / np.abs(ref).max(axis=(0, 2))
