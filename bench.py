@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--no-chunks", action="store_true",
                     help="skip timing the step with head-chunked attention and overlapped output exchange")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--ulysses", choices=["a2a", "ag"], default=None,
+                    help="time the Ulysses step ACROSS ranks instead (one sequence, S/N rows per rank, strong "
+                         "scaling): a2a = all-to-all of q, k, v; ag = all-gather of the fp8 hidden state")
     return ap.parse_args()
 
 
@@ -206,6 +209,7 @@ def dist_setup(args):
     if world > 1:
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
         backend = "nccl" if args.impl == "h3attn" else "gloo"
         if backend == "nccl":
             torch.cuda.set_device(local)
@@ -421,11 +425,114 @@ def make_inputs(w, dev, rank):
                  for seed in (synth.SEED_Q, synth.SEED_K, synth.SEED_V))
 
 
+def run_ulysses_across_ranks(args, world, rank, local):
+    """--ulysses: one packed sequence split over the N ranks (rows
+    [r*S/N, (r+1)*S/N) on rank r), one step = the distributed Ulysses step of
+    every rank (all-to-all or all-gather form); `value` = the sequence's
+    attention TFLOP/s over the max-over-ranks time (strong scaling).  A single
+    process runs it as a one-rank group, which times the collective path."""
+    import datetime
+    import socket
+    import torch
+    import torch.distributed as dist
+    import dit_sequence_attention_gb300 as h3
+    from dit_sequence_attention_gb300 import synth
+    from dit_sequence_attention_gb300.ulysses import UlyssesGroup
+
+    h3.load_library()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if world == 1:
+        os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                                timeout=datetime.timedelta(seconds=300))
+    g = UlyssesGroup()
+    P = g.P
+    w = synth.WORKLOADS[args.workload]
+    S, H, D = w.S, w.H, w.D
+    if S % (P * P) or H % P:
+        raise SystemExit(f"--ulysses needs P={P} to divide H and S/P (S={S}, H={H})")
+    S_loc = S // P
+    rows = slice(g.rank * S_loc, (g.rank + 1) * S_loc)
+    wq, wk = (t.to(dev) for t in synth.norm_weights(D))
+    pos = torch.from_numpy(synth.packed_positions(w)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    if args.ulysses == "a2a":
+        q, k, v = (t[rows].contiguous() for t in synth.qkv(w, dev))   # the same sequence on every rank
+        pos_loc = pos[rows].contiguous()
+        work = g.make_workspace(S_loc, H, D, dev)
+
+        def step():
+            g.attention_step(q, k, v, wq, wk, pos_loc, w.S_v, *w.rope_split, w.eps, w.theta, work=work,
+                             stream=stream)
+        # each rank receives (P-1)/P of its head group's q, k, v rows and of its output rows
+        recv_bytes = (3 + 1) * S_loc * H * D * 2 * (P - 1) // P
+    else:
+        hidden = synth.HIDDEN
+        x = synth.fp8_e4m3_codes((S, hidden), 61, 1.0, dev)[rows].contiguous()
+        wt = synth.fp8_e4m3_codes((3 * H * D, hidden), 62, 4.0, dev)
+        sc = 1.0 / (4.0 * hidden ** 0.5)
+        work = g.make_workspace(S_loc, H, D, dev, hidden=hidden)
+
+        def step():
+            g.attention_step_allgather(x, wt, sc, wq, wk, pos, w.S_v, *w.rope_split, w.eps, w.theta, work=work,
+                                       stream=stream)
+        # each rank receives the other ranks' fp8 hidden rows and (P-1)/P of its output rows
+        recv_bytes = (P - 1) * S_loc * hidden + S_loc * H * D * 2 * (P - 1) // P
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if h3.h3attn_get_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clk = clocks.stop()
+    if h3.h3attn_get_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+    t = a.elapsed_time(b)
+    tt = torch.tensor([t], dtype=torch.float64, device=dev)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    ms = float(tt.item())
+    dist.destroy_process_group()
+    if rank != 0:
+        return
+    value = w.attention_flops() * args.steps / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v or fp8 hidden, random-init "
+        "weights)",
+        "config": dict(workload_config(w, P), exchange=args.ulysses, parallelism=f"ulysses{P}",
+                       received_bytes_per_rank_per_step=recv_bytes),
+        "tokens_per_s": w.S_v * args.steps / (ms * 1e-3),
+        "clocks": clk,
+        "gpu_launches": args.steps * 4,   # this library's kernels per step (the collectives are NCCL's)
+        "note": "one sequence over all ranks; every rank's step includes its collectives (NCCL)",
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.ulysses is not None:
+        run_ulysses_across_ranks(args, world, rank, local)
         return
     import torch
     import dit_sequence_attention_gb300 as h3
