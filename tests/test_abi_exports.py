@@ -145,3 +145,25 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
         monkeypatch.setattr(h3, "_debug", debug)
         with pytest.raises(RuntimeError, match="not built"):
             h3.load_library()
+
+
+def test_header_compiles_as_c_and_the_abi_links_from_c(lib, tmp_path):
+    """A C99 program includes include/h3attn.h, links libh3attn.so and calls
+    the entry points that need no GPU (version, strings, flags, argument
+    checks that refuse a call before any CUDA work)."""
+    import shutil
+    import subprocess
+    import dit_sequence_attention_gb300 as h3
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(h3.library_path())
+    exe = str(tmp_path / "abi_from_c")
+    src = os.path.join(ROOT, "tests", "c", "abi_from_c.c")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), src,
+                        "-o", exe, "-L", libdir, "-l:libh3attn.so", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert "abi_from_c ok" in r.stdout
