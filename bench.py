@@ -575,9 +575,10 @@ def main():
 
     # ---------------------------------------------------------------- e2e
     # Through the public API from pinned host buffers: every step copies its
-    # q, k, v and positions host->device and its output device->host.  Copies
-    # run on a second stream, double-buffered, so the H2D of step i+1 and the
-    # D2H of step i overlap the compute of step i (as a streaming caller would).
+    # q, k, v and positions host->device and its output device->host.  The two
+    # directions run on streams of their own, double-buffered, so the inputs of
+    # step i+1 arrive and the output of step i-1 leaves while step i computes
+    # (as a streaming caller would).
     e2e_steps = args.e2e_steps or max(2, args.steps)   # the same stream length as the device-timed region
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     hpos = pos.cpu().pin_memory()
@@ -585,45 +586,48 @@ def main():
     dins = [(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(pos))
             for _ in range(2)]
     works = [work, h3.make_workspace(S, H, D, P, dev)]
-    copy = torch.cuda.Stream(dev)
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_run(n):
+    def fetch(b):
+        for t_dev, t_host in zip(dins[b], (hq, hk, hv, hpos)):
+            t_dev.copy_(t_host, non_blocking=True)
+        ev_in[b].record(h2d_s)
+
+    def e2e_run(n, ev_first=None):
         for b in range(2):
-            ev_out[b].record(copy)
-        with torch.cuda.stream(copy):
-            for t_dev, t_host in zip(dins[0], (hq, hk, hv, hpos)):
-                t_dev.copy_(t_host, non_blocking=True)
-            ev_in[0].record(copy)
+            ev_out[b].record(d2h_s)             # both output buffers are free
+        with torch.cuda.stream(h2d_s):
+            if ev_first is not None:
+                ev_first.record(h2d_s)
+            fetch(0)
         for i in range(n):
             b = i % 2
+            if i + 1 < n:
+                nb = (i + 1) % 2
+                with torch.cuda.stream(h2d_s):
+                    if i >= 1:
+                        h2d_s.wait_event(ev_done[nb])   # step i-1 finished reading these inputs
+                    fetch(nb)
             stream.wait_event(ev_in[b])
-            stream.wait_event(ev_out[b])          # previous D2H of this output buffer done
+            stream.wait_event(ev_out[b])                 # the output of step i-2 has left this buffer
             dq_, dk_, dv_, dp_ = dins[b]
             o = h3.ulysses_attention_step(dq_, dk_, dv_, wq, wk, dp_, P, w.S_v, *w.rope_split, w.eps, w.theta,
                                           work=works[b], stream=stream)
             ev_done[b].record(stream)
-            with torch.cuda.stream(copy):
-                if i + 1 < n:
-                    nb = (i + 1) % 2
-                    if i >= 1:
-                        copy.wait_event(ev_done[nb])  # step i-1 finished reading these inputs
-                    for t_dev, t_host in zip(dins[nb], (hq, hk, hv, hpos)):
-                        t_dev.copy_(t_host, non_blocking=True)
-                    ev_in[nb].record(copy)
-                copy.wait_event(ev_done[b])
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(ev_done[b])
                 hout[b].copy_(o, non_blocking=True)
-                ev_out[b].record(copy)
+                ev_out[b].record(d2h_s)
 
     e2e_run(2)
     torch.cuda.synchronize(dev)
     barrier()
     ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev_a.record(copy)
-    e2e_run(e2e_steps)
-    ev_b.record(copy)
+    e2e_run(e2e_steps, ev_first=ev_a)       # ev_a: before the first input copy
+    ev_b.record(d2h_s)                      # after the last output copy (which follows every step)
     torch.cuda.synchronize(dev)
     barrier()
     if h3.h3attn_get_device_status() != 0:
@@ -632,6 +636,16 @@ def main():
     e2e_value = job_tflops(flops_seq, e2e_steps, world, e2e_ms)
     h2d = 3 * tensor_bytes + hpos.numel() * 4
     d2h = tensor_bytes
+
+    def copy_gbs(dst, src, st):
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            ea.record(st)
+            dst.copy_(src, non_blocking=True)
+            eb.record(st)
+        torch.cuda.synchronize(dev)
+        return src.numel() * src.element_size() / (ea.elapsed_time(eb) * 1e-3) / 1e9
+    link = {"h2d_GB_per_s": copy_gbs(dins[0][0], hq, h2d_s), "d2h_GB_per_s": copy_gbs(hout[0], works[0]["o"], d2h_s)}
     del hq, hk, hv, hout, dins, works
 
     # --------------------------------------- the 262k end of the metric: 1080p
@@ -770,9 +784,10 @@ def main():
         "kernels": kernels,
         "hbm_peak_GB_per_s": peaks["hbm_gbs"],
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps, "copy_link": link,
                 "note": "pinned host q/k/v/pos -> device, whole path, device -> pinned host output each step; "
-                        "copies double-buffered on a second stream, overlapping compute"},
+                        "each direction double-buffered on its own stream, overlapping compute; copy_link = one "
+                        "734 MB copy each way measured alone"},
         "gpu_launches": args.steps * runner.launches_per_step(),
         "clocks": clk,
         "workloads": long_leg,
