@@ -1,4 +1,4 @@
-"""Ulysses sequence parallelism across ranks: the all-to-all exchanges.
+"""Ulysses sequence parallelism across ranks: the all-to-all and all-gather forms.
 
 "buqi-minimax-h3-multigpu" README, "How it works": every rank keeps a
 row-shard of the packed sequence for the per-token work (QK-norm, RoPE); for
@@ -208,6 +208,8 @@ class UlyssesGroup:
             raise ValueError(f"P={P} must divide H={H} and the shard length S/P={S_loc}")
         if work is None:
             work = self.make_workspace(S_loc, H, D, x_local.device, hidden=hidden)
+        elif "x" not in work:
+            raise ValueError("the workspace of the all-gather form needs make_workspace(..., hidden=...)")
         if stream is None:
             stream = torch.cuda.current_stream(x_local.device)
         with torch.cuda.stream(stream):
