@@ -297,11 +297,16 @@ def h3attn_qkv_proj_fp8(x_fp8, w_fp8, scale, q_out, k_out, v_out, P, rank, strea
 
 
 def h3attn_get_device_status(stream=None) -> int:
-    """Synchronise the stream and return (and clear) the device status code (0 = ok)."""
+    """Take the current device's status word (read and clear it in one atomic
+    exchange, ordered after the work already on `stream`), synchronise
+    `stream`, and return the status code (0 = ok).  An error recorded by a
+    kernel on another stream is returned by this call or by the next one."""
     return int(load_library().h3attn_get_device_status(_stream_ptr(stream)))
 
 
 def h3attn_last_device_error_info() -> int:
+    """Diagnostic word of the last device error taken on the current device
+    (kernel tag << 32 | site << 16 | low index bits), 0 if none."""
     return int(load_library().h3attn_last_device_error_info())
 
 
