@@ -267,3 +267,55 @@ def test_ulysses_group_without_process_group():
     for bad in (-1, 4):
         with pytest.raises(ValueError):
             UlyssesGroup(P=4, rank=bad)
+
+
+# --------------------------------------------- a rank that fails mid-step
+def _failing_peer_worker(rank, world, port, out, mode="exits"):
+    """Rank 1 fails before the sequence->heads exchange -- it exits ("exits")
+    or stays alive without ever joining the collective ("stalls") -- and
+    rank 0, inside the exchange, must get an error (the lost connection, or
+    the process group's 5 s timeout) instead of waiting forever."""
+    import datetime
+    import time
+
+    import torch
+    sys.path.insert(0, ROOT)
+    from dit_sequence_attention_gb300.ulysses import UlyssesGroup
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=5))
+    ug = UlyssesGroup()
+    send = torch.zeros((world, 4, 2, 64), dtype=torch.bfloat16)
+    if rank == 1:
+        out[rank] = "left"
+        if mode == "stalls":
+            time.sleep(20)                       # alive, but never joins the exchange
+        os._exit(0)                              # gone, without a clean shutdown
+    t0 = time.monotonic()
+    try:
+        ug.exchange(send)
+        out[rank] = ("no error", time.monotonic() - t0)
+    except Exception as e:                       # gloo reports the lost peer or the timeout
+        out[rank] = (type(e).__name__, time.monotonic() - t0)
+    os._exit(0)
+
+
+@pytest.mark.parametrize("mode", ["exits", "stalls"])
+def test_exchange_with_a_lost_peer_fails_instead_of_hanging(mode):
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with mp.Manager() as m:
+        out = m.dict()
+        procs = [ctx.Process(target=_failing_peer_worker, args=(r, 2, port, out, mode)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=120)
+        alive = [p for p in procs if p.is_alive()]
+        for p in alive:
+            p.kill()
+        res = dict(out)
+    assert not alive, "a rank was still waiting after 120 s"
+    assert res.get(1) == "left"
+    kind, seconds = res[0]
+    assert kind != "no error", "the exchange completed without its peer"
+    assert seconds < 15, f"the error took {seconds:.1f} s (process-group timeout 5 s)"
