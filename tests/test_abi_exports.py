@@ -167,3 +167,36 @@ def test_header_compiles_as_c_and_the_abi_links_from_c(lib, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stderr
     assert "abi_from_c ok" in r.stdout
+
+
+def test_empty_and_oversized_inputs_are_refused_before_any_cuda_call(lib):
+    """Empty sizes (S, B, H or a head count of 0) and sizes past the kernels'
+    index limits are H3ATTN_ERR_SHAPE; nothing is launched (no GPU needed)."""
+    import dit_sequence_attention_gb300 as h3
+    null = None
+    a, b, c, d = 0x10000, 0x10000000, 0x20000000, 0x30000000   # aligned, never dereferenced
+    SHAPE = h3.H3ATTN_ERR_SHAPE
+    # attention: no rows, no batch items, no heads, an empty head range, more heads than one grid row holds
+    for B, S, H, hb, hc in ((1, 0, 4, 0, 4), (0, 256, 4, 0, 4), (1, 256, 0, 0, 1), (1, 256, 4, 0, 0),
+                            (1, 256, 70000, 0, 65536)):
+        assert lib.h3attn_forward(a, b, c, d, B, S, H, 64, hb, hc, null, 0.0, null) == SHAPE, (B, S, H, hb, hc)
+    # layout exchanges: no rows / heads, and more 16-byte vectors than a 32-bit index reaches
+    assert lib.h3attn_seq2head(a, b, 0, 56, 128, 2, null) == SHAPE
+    assert lib.h3attn_head2seq(a, b, 64, 0, 128, 1, null) == SHAPE
+    assert lib.h3attn_seq2head(a, b, 1 << 20, 1024, 128, 2, null) == SHAPE
+    assert lib.h3attn_head2seq(a, b, 1 << 20, 1024, 128, 2, null) == SHAPE
+    assert lib.h3attn_head2seq_heads(a, b, 64, 56, 128, 2, 0, 0, 0, null) == SHAPE
+    assert lib.h3attn_head2seq_heads(a, b, 1 << 20, 1024, 128, 2, 0, 0, 1, null) == SHAPE
+    # norm/RoPE: no rows, no batch items, no heads
+    norm = lib.h3attn_qk_norm_rope
+    for B, S, H in ((1, 0, 4), (0, 16, 4), (1, 16, 0)):
+        assert norm(a, a + 0x100000, b, b + 0x100000, null, c, c + 0x1000, d, B, S, H, 64, 16, 24, 24, 1e-6, 1e4,
+                    null) == SHAPE, (B, S, H)
+    assert lib.h3attn_qk_norm_rope_seq2head(a, a + 0x100000, b, b + 0x100000, null, c, c + 0x1000, d, 0, 56, 128,
+                                            2, 32, 48, 48, 1e-6, 1e4, null) == SHAPE
+    # projection: no rows, hidden not a multiple of 16, a rank slice not a multiple of 8 columns, rank >= P
+    proj = lib.h3attn_qkv_proj_fp8
+    for S, hidden, inner, P, rank in ((0, 64, 512, 2, 0), (16, 40, 512, 2, 0), (16, 64, 516, 2, 0),
+                                      (16, 64, 512, 2, 2), (16, 64, 512, 0, 0)):
+        assert proj(a, b, 1.0, c, c + 0x1000000, c + 0x2000000, S, hidden, inner, P, rank, null) == SHAPE, \
+            (S, hidden, inner, P, rank)
