@@ -347,8 +347,12 @@ def ulysses_attention_step(q, k, v, w_q, w_k, pos, P, kv_len, d_t, d_h, d_w, eps
       chunk count).  `work` may pass preallocated buffers (make_workspace).
     """
     S, H, D = q.shape
+    if int(attn_chunks) != attn_chunks or attn_chunks < 1:
+        raise ValueError(f"attn_chunks must be a positive integer, got {attn_chunks}")
     if work is None:
         work = make_workspace(S, H, D, P, q.device, fused=fused)
+    elif not fused and not ("qr" in work and "kr" in work):
+        raise ValueError("the unfused step needs a workspace from make_workspace(..., fused=False)")
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     if fused:

@@ -200,3 +200,22 @@ def test_empty_and_oversized_inputs_are_refused_before_any_cuda_call(lib):
                                       (16, 64, 512, 2, 2), (16, 64, 512, 0, 0)):
         assert proj(a, b, 1.0, c, c + 0x1000000, c + 0x2000000, S, hidden, inner, P, rank, null) == SHAPE, \
             (S, hidden, inner, P, rank)
+
+
+def test_step_arguments_are_checked_before_any_launch():
+    """A chunk count below one, or an unfused step handed the fused workspace,
+    is refused before anything is allocated or launched (CPU tensors: a call
+    that got as far as a kernel would fail on the device check instead)."""
+    import torch
+    import dit_sequence_attention_gb300 as h3
+    S, H, D, P = 16, 4, 64, 2
+    q = k = v = torch.zeros((S, H, D), dtype=torch.bfloat16)
+    w = torch.ones(D)
+    pos = torch.zeros((S, 3), dtype=torch.int32)
+    for chunks in (0, -1, 1.5):
+        with pytest.raises(ValueError, match="attn_chunks"):
+            h3.ulysses_attention_step(q, k, v, w, w, pos, P, S, 16, 24, 24, attn_chunks=chunks,
+                                      exchange_stream=object())
+    fused_work = {name: None for name in ("qh", "kh", "vh", "oh", "o")}
+    with pytest.raises(ValueError, match="unfused"):
+        h3.ulysses_attention_step(q, k, v, w, w, pos, P, S, 16, 24, 24, work=fused_work, fused=False)
