@@ -124,7 +124,9 @@ H3ATTN_API int h3attn_qk_norm_rope_seq2head(const void* q, const void* k, void* 
  *               It is read on the host during the call; a device pointer is
  *               refused with H3ATTN_ERR_ARG before it is touched.
  *               Rows >= kv_len[b] of k and v are never read (NaN there is fine).
- *   scale       softmax scale; <= 0 selects 1/sqrt(D).
+ *   scale       softmax scale; <= 0 selects 1/sqrt(D); NaN is refused (H3ATTN_ERR_ARG).
+ *   B >= 1, S >= 1, 0 <= head_begin, 1 <= head_count <= 65535 and
+ *   head_begin + head_count <= H_buf (H3ATTN_ERR_SHAPE otherwise).
  * The per-head result does not depend on head_begin/head_count or on how many
  * heads one call covers: splitting the heads over several calls gives
  * bit-identical output.
