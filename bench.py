@@ -144,7 +144,7 @@ def read_traffic():
 class ClockSampler:
     """nvidia-smi clock / throttle-reason sampling during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -176,11 +176,19 @@ class ClockSampler:
         with open(self.path) as f:
             text = f.read()
         os.unlink(self.path)
+        return self.summarize(text)
+
+    @staticmethod
+    def summarize(text):
+        """Median SM clock, median instantaneous board power and the throttle
+        reasons seen in nvidia-smi's CSV output; None without a usable sample.
+        (The plain power.draw field is a one-second average, which lags a
+        timed region of about a second.)"""
         rows = list(csv.reader(io.StringIO(text)))
         if len(rows) < 2:
             return None
         hdr = [h.strip() for h in rows[0]]
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows[1:]:
             if len(r) != len(hdr):
@@ -191,14 +199,21 @@ class ClockSampler:
                 smax.append(float(rec[[h for h in hdr if h.startswith("clocks.max.sm")][0]].split()[0]))
             except Exception:
                 continue
+            try:
+                power.append(float(rec[[h for h in hdr if h.startswith("power.draw")][0]].split()[0]))
+            except Exception:
+                pass
             for n in names:
                 key = [h for h in hdr if h.startswith(f"clocks_event_reasons.{n}")]
                 if key and rec[key[0]].lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if power:
+            out["power_w"] = statistics.median(power)
+        return out
 
 
 def dist_setup(args):
@@ -624,12 +639,16 @@ def main():
 
     e2e_run(2)
     torch.cuda.synchronize(dev)
+    e2e_clocks = ClockSampler(local)
+    e2e_clocks.start()
+    time.sleep(0.3)
     barrier()
     ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_run(e2e_steps, ev_first=ev_a)       # ev_a: before the first input copy
     ev_b.record(d2h_s)                      # after the last output copy (which follows every step)
     torch.cuda.synchronize(dev)
     barrier()
+    e2e_clk = e2e_clocks.stop()
     if h3.h3attn_get_device_status() != 0:
         raise RuntimeError("device status error in the end-to-end loop")
     e2e_ms = max_over_ranks(ev_a.elapsed_time(ev_b), world, dev)
@@ -784,7 +803,7 @@ def main():
         "kernels": kernels,
         "hbm_peak_GB_per_s": peaks["hbm_gbs"],
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps, "copy_link": link,
+                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps, "copy_link": link, "clocks": e2e_clk,
                 "note": "pinned host q/k/v/pos -> device, whole path, device -> pinned host output each step; "
                         "each direction double-buffered on its own stream, overlapping compute; copy_link = one "
                         "734 MB copy each way measured alone"},

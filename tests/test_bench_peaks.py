@@ -68,3 +68,21 @@ def test_committed_traffic_capture_matches_the_current_sources():
     if the kernel changes, the capture has to be taken again."""
     traffic, src = bench.read_traffic()
     assert traffic is not None and traffic > 4 * 51200 * 28 * 128 * 2, src
+
+
+def test_clock_summary_of_an_nvidia_smi_capture():
+    """Median clock and power, and every throttle reason that was active in
+    any sample; rows that do not parse are skipped."""
+    hdr = ("index, clocks.current.sm [MHz], clocks.max.sm [MHz], power.draw.instant [W], clocks_event_reasons.active, "
+           "clocks_event_reasons.hw_slowdown, clocks_event_reasons.hw_thermal_slowdown, "
+           "clocks_event_reasons.sw_thermal_slowdown, clocks_event_reasons.sw_power_cap")
+    rows = ["0, 1897 MHz, 2070 MHz, 1240.50 W, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 1905 MHz, 2070 MHz, 1251.00 W, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 1850 MHz, 2070 MHz, 1238.25 W, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, [N/A], 2070 MHz, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active",
+            "truncated, row"]
+    out = bench.ClockSampler.summarize("\n".join([hdr] + rows) + "\n")
+    assert out == {"sm_mhz": 1897.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3,
+                   "power_w": 1240.5}
+    assert bench.ClockSampler.summarize(hdr + "\n") is None
+    assert bench.ClockSampler.summarize("") is None
